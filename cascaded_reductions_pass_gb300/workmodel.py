@@ -1,0 +1,50 @@
+"""Algorithmic work of each operation: the bytes and flops the method must move
+or compute, independent of how a kernel does it.  Used for roofline figures.
+
+Byte counts are the compulsory HBM traffic of the fused single-loop form: every
+input read once, every output written once ("Operator Fusion" guide, section 1:
+a fused residual + LayerNorm reads x and the residual and writes the output,
+2 reads + 1 write).  Flop counts follow the FlashAttention convention: 4*D
+flops per visible (query, key) pair (two multiply-adds per element of Q K^T and
+of P V); a causal mask counts half the square.
+"""
+from __future__ import annotations
+
+ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2}
+
+
+def attn_flops(B, Hq, Nq, Nk, D, causal):
+    full = 4.0 * B * Hq * Nq * Nk * D
+    return full / 2.0 if causal else full
+
+
+def attn_bytes(B, Hq, Hkv, Nq, Nk, D, dtype, with_lse=True):
+    e = ELEM_BYTES[dtype]
+    q = B * Hq * Nq * D * e
+    kv = 2 * B * Hkv * Nk * D * e
+    o = B * Hq * Nq * D * e
+    lse = B * Hq * Nq * 4 if with_lse else 0
+    return q + kv + o + lse
+
+
+def decode_bytes(B, Hq, Hkv, L, D, dtype, with_lse=True):
+    """K and V caches read once, q read once, O (and LSE) written once.  The
+    fp32 split partials' round trip through the workspace is not credited."""
+    return attn_bytes(B, Hq, Hkv, 1, L, D, dtype, with_lse)
+
+
+def decode_flops(B, Hq, L, D):
+    return attn_flops(B, Hq, 1, L, D, False)
+
+
+def merge_bytes(rows, num_splits, D, out_dtype, with_lse=True):
+    """Partials read once (fp32 O_s and lse_s), merged O (and LSE) written once."""
+    return rows * num_splits * (D + 1) * 4 + rows * D * ELEM_BYTES[out_dtype] + (rows * 4 if with_lse else 0)
+
+
+def layernorm_bytes(rows, cols, dtype, affine=True, residual_out=False):
+    """x and residual read once, y written once (+ h if residual_out); gamma and
+    beta read once per call."""
+    e = ELEM_BYTES[dtype]
+    t = rows * cols * e
+    return 3 * t + (t if residual_out else 0) + (2 * cols * e if affine else 0)

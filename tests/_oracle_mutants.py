@@ -1,0 +1,44 @@
+"""Planted mistakes in the oracle, used to show that its pins catch them.
+
+Each mutant is one plausible slip in ``oracle/reference.py`` (a dropped term,
+a wrong sign or index, a transposed operand, the other variance divisor...).
+``apply(name)`` rewrites the oracle module in memory -- on the CPU, in the
+test process only -- and ``test_oracle_mutants.py`` runs the oracle pin suite
+under each mutant, expecting it to fail.
+"""
+import importlib
+import inspect
+
+# name -> (exact snippet in oracle/reference.py, its mutated replacement)
+MUTANTS = {
+    "attn_scale_dropped": ("* scale\n", "* 1.0\n"),
+    "attn_causal_off_by_one": ("key_idx <= sel[:, None]", "key_idx < sel[:, None] + 2"),
+    "attn_gqa_map_modulo": ("kvh = h // group", "kvh = h % Hkv"),
+    "attn_k_for_v": ("acc = p @ v[b, kvh]", "acc = p @ k[b, kvh][:, :Dv]"),
+    "attn_lse_missing_max": ("m_safe + np.log(l), NEG_INF", "np.log(l), NEG_INF"),
+    "attn_not_normalised": ("acc / l[:, None]", "acc / l.max()"),
+    "attn_exp_sign": ("p = np.exp(s - m_safe[:, None])", "p = np.exp(m_safe[:, None] - s)"),
+    "split_bounds_overlap": ("((s + 1) * L) // num_splits)", "((s + 1) * L) // num_splits + 1)"),
+    "merge_weight_not_normalised": ("np.exp(lse_part - np.where(live, lse, 0.0)[..., None])",
+                                    "np.exp(lse_part - np.where(live, mx_safe, 0.0)[..., None])"),
+    "merge_lse_missing_max": ("lse = np.where(live, mx_safe + np.log(total), NEG_INF)",
+                              "lse = np.where(live, np.log(total), NEG_INF)"),
+    "ln_unbiased_variance": ("keepdims=True) / n  # pass 2", "keepdims=True) / (n - 1)  # pass 2"),
+    "ln_eps_outside_sqrt": ("np.sqrt(var + eps)", "(np.sqrt(var) + eps)"),
+    "ln_residual_dropped": ("h = x + r ", "h = x + 0 * r "),
+    "ln_beta_scaled": ("* g + b ", "* (g + b) "),
+}
+
+
+def apply(name):
+    import oracle
+    import oracle.reference as ref
+
+    old, new = MUTANTS[name]
+    src = inspect.getsource(importlib.import_module("oracle.reference"))
+    if src.count(old) != 1:
+        raise RuntimeError(f"mutant {name}: snippet found {src.count(old)} times")
+    code = compile(src.replace(old, new), ref.__file__, "exec")
+    exec(code, ref.__dict__)
+    for fn in ("attention", "decode", "decode_partials", "layernorm", "lse_merge", "split_bounds"):
+        setattr(oracle, fn, getattr(ref, fn))

@@ -1,0 +1,128 @@
+"""Pins for the residual + LayerNorm oracle (CPU only).
+
+Definition: "Operator Fusion" guide, section 2, Pattern 2 (mean -> variance ->
+normalise) and section 4 (residual added first, eps inside the square root,
+biased variance, affine gamma/beta).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+
+def _rand(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+def brute_ln(x, r, g, b, eps):
+    y = np.zeros_like(x)
+    for i in range(x.shape[0]):
+        h = [x[i, j] + r[i, j] for j in range(x.shape[1])]
+        n = len(h)
+        mu = math.fsum(h) / n
+        var = math.fsum((t - mu) ** 2 for t in h) / n
+        for j in range(n):
+            y[i, j] = (h[j] - mu) / math.sqrt(var + eps) * g[j] + b[j]
+    return y
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 1), (3, 7), (4, 16), (2, 33)])
+def test_brute_force(rows, cols):
+    x, r = _rand((rows, cols), 1), _rand((rows, cols), 2)
+    g, b = _rand((cols,), 3), _rand((cols,), 4)
+    y, h = oracle.layernorm(x, r, g, b, 1e-5)
+    np.testing.assert_allclose(y, brute_ln(x, r, g, b, 1e-5), atol=1e-12)
+    np.testing.assert_array_equal(h, x + r)
+
+
+def test_pre_affine_mean_zero_biased_variance():
+    x, r = _rand((8, 64), 5) * 3 + 1, _rand((8, 64), 6)
+    eps = 1e-5
+    y, h = oracle.layernorm(x, r, np.ones(64), np.zeros(64), eps)
+    np.testing.assert_allclose(y.mean(-1), 0.0, atol=1e-12)
+    var = h.var(-1)  # numpy default ddof=0: biased
+    np.testing.assert_allclose((y ** 2).mean(-1), var / (var + eps), atol=1e-12)
+
+
+def test_constant_row_gives_beta():
+    x = np.full((2, 10), 3.25)
+    r = np.full((2, 10), -1.0)
+    g, b = _rand((10,), 7), _rand((10,), 8)
+    y, _ = oracle.layernorm(x, r, g, b, 1e-5)
+    np.testing.assert_allclose(y, np.broadcast_to(b, y.shape), atol=1e-12)
+
+
+def test_plus_minus_a_row():
+    a, eps = 0.7, 1e-3
+    x = np.array([[a, -a, a, -a, -a, a]])
+    g, b = _rand((6,), 9), _rand((6,), 10)
+    y, _ = oracle.layernorm(x, np.zeros_like(x), g, b, eps)
+    np.testing.assert_allclose(y[0], np.sign(x[0]) * a / math.sqrt(a * a + eps) * g + b, atol=1e-12)
+
+
+def test_shift_invariance():
+    x, r = _rand((3, 20), 11), _rand((3, 20), 12)
+    g, b = _rand((20,), 13), _rand((20,), 14)
+    y1, _ = oracle.layernorm(x, r, g, b, 1e-5)
+    y2, _ = oracle.layernorm(x + 5.0, r, g, b, 1e-5)
+    np.testing.assert_allclose(y1, y2, atol=1e-11)
+
+
+def test_residual_is_added_not_swapped():
+    # The residual and x enter symmetrically through h = x + r; swapping them must
+    # not change y, while dropping r must.
+    x, r = _rand((2, 12), 15), _rand((2, 12), 16)
+    g, b = np.ones(12), np.zeros(12)
+    y1, _ = oracle.layernorm(x, r, g, b, 1e-5)
+    y2, _ = oracle.layernorm(r, x, g, b, 1e-5)
+    y3, _ = oracle.layernorm(x, 0 * r, g, b, 1e-5)
+    np.testing.assert_allclose(y1, y2, atol=1e-12)
+    assert np.abs(y1 - y3).max() > 0.1
+
+
+def test_torch_layer_norm_second_opinion():
+    x = torch.randn(5, 48, dtype=torch.float64, generator=torch.Generator().manual_seed(0))
+    r = torch.randn(5, 48, dtype=torch.float64, generator=torch.Generator().manual_seed(1))
+    g = torch.rand(48, dtype=torch.float64, generator=torch.Generator().manual_seed(2)) + 0.5
+    b = torch.randn(48, dtype=torch.float64, generator=torch.Generator().manual_seed(3)) * 0.1
+    ref = torch.nn.functional.layer_norm(x + r, (48,), g, b, eps=1e-5)
+    y, _ = oracle.layernorm(x.numpy(), r.numpy(), g.numpy(), b.numpy(), 1e-5)
+    np.testing.assert_allclose(y, ref.numpy(), atol=1e-12)
+
+
+def test_welford_chan_incremental_form_reaches_plain_result():
+    """The incremental form (RedFuser, Figure 4) of mean -> M2: Welford's update
+    per element and Chan et al.'s pairwise combine of partial (n, mean, M2),
+    written here in fp64, reaches the oracle's plain two-pass statistics."""
+    x = _rand((1, 101), 17) * 4 + 10
+    r = np.zeros_like(x)
+    y, h = oracle.layernorm(x, r, np.ones(101), np.zeros(101), 1e-5)
+
+    def welford(vals):
+        n, mean, m2 = 0, 0.0, 0.0
+        for t in vals:
+            n += 1
+            d = t - mean
+            mean += d / n
+            m2 += d * (t - mean)
+        return n, mean, m2
+
+    def chan(a, b):
+        na, ma, qa = a
+        nb, mb, qb = b
+        n = na + nb
+        if n == 0:
+            return 0, 0.0, 0.0
+        d = mb - ma
+        return n, ma + d * nb / n, qa + qb + d * d * na * nb / n
+
+    parts = [welford(h[0, i:i + 13]) for i in range(0, 101, 13)] + [welford([])]
+    tot = parts[0]
+    for p in parts[1:]:
+        tot = chan(tot, p)
+    n, mean, m2 = tot
+    yy = (h[0] - mean) / math.sqrt(m2 / n + 1e-5)
+    np.testing.assert_allclose(yy, y[0], atol=1e-12)
