@@ -1,0 +1,450 @@
+"""Benchmark of the fused cascaded-reduction kernels on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one call of the hot path on one batch of the workload's synthetic
+input, inputs already resident in HBM.  The default workload is the
+non-causal fp16 attention forward (B=4 H=12 N=4096 D=64, seed 1); the line's
+``parts`` object reports the other workloads (causal GQA bf16 attention,
+split-KV decode, residual+LayerNorm, tiny fp32 attention) measured the same
+way in the same run.  Each timed step is bracketed by CUDA events on the
+launching stream, with an L2 flush (a 512 MiB memset, larger than the 129 MB
+L2) before every step, outside the events.  Under torchrun each rank runs an
+independent replica (no data-path collective: the work of one call does not
+shard across GPUs here), ``value`` is the units all ranks processed divided by
+the slowest rank's time.
+
+``--impl reference`` times the fp64 CPU oracle (a deliberately slow baseline,
+not a GPU reference implementation) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from cascaded_reductions_pass_gb300 import inputs, workmodel  # noqa: E402
+
+L2_FLUSH_BYTES = 512 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_traffic(kernel_file, workload):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source
+    is unchanged since the counters were taken; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        table = json.load(f)
+    ent = table.get(workload)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "cascaded_reductions_pass_gb300", "csrc", kernel_file)
+    with open(src, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    return ent["bytes_per_launch"] if ent.get("source_sha256_16") == digest else None
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 7:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        sel = [p for (t, p) in self.samples if t0 - 0.25 <= t <= t1 + 0.25] or [p for (_, p) in self.samples]
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(p[0]) for p in sel if p[0].replace(".", "").isdigit()]
+        mx = [float(p[1]) for p in sel if p[1].replace(".", "").isdigit()]
+        reasons = sorted({self.NAMES[i] for p in sel for i in range(4) if p[3 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(sel)}
+
+
+# ----------------------------------------------------------------------------- workloads
+class Runner:
+    """One workload: its inputs on the device, one step of the hot path, its work."""
+
+    def __init__(self, name, dev):
+        import cascaded_reductions_pass_gb300 as rf
+
+        self.rf = rf
+        self.w = inputs.WORKLOADS[name]
+        self.dev = dev
+        d = self.w.dims
+        self.host = inputs.make(self.w)
+        self.dtype = self.w.dtype
+        if self.w.kind == "attn":
+            self.scale = float(np.float32(1.0 / math.sqrt(d["D"])))
+            self.flops = workmodel.attn_flops(d["B"], d["Hq"], d["N"], d["N"], d["D"], d["causal"])
+            self.bytes = workmodel.attn_bytes(d["B"], d["Hq"], d["Hkv"], d["N"], d["N"], d["D"], self.dtype)
+            self.metric, self.unit, self.bound = "attention forward TFLOP/s", "TFLOP/s", "tensor"
+            self.units = self.flops / 1e12
+            self.kernel_file = "attn_fwd_f32.cu" if self.dtype == "f32" else "attn_fwd_tc.cu"
+            self.kernel = "attn_fwd_f32" if self.dtype == "f32" else "attn_fwd_tc"
+            if self.dtype == "f32":
+                self.bound = "alu"
+        elif self.w.kind == "decode":
+            self.scale = float(np.float32(1.0 / math.sqrt(d["D"])))
+            self.bytes = workmodel.decode_bytes(d["B"], d["Hq"], d["Hkv"], d["L"], d["D"], self.dtype)
+            self.flops = workmodel.decode_flops(d["B"], d["Hq"], d["L"], d["D"])
+            self.metric, self.unit, self.bound = "split-KV decode GB/s", "GB/s", "hbm"
+            self.units = self.bytes / 1e9
+            self.kernel_file, self.kernel = "decode_split.cu", "decode_split (+ lse_merge)"
+        else:
+            self.bytes = workmodel.layernorm_bytes(d["rows"], d["cols"], self.dtype)
+            self.flops = 10.0 * d["rows"] * d["cols"]
+            self.metric, self.unit, self.bound = "residual+LayerNorm GB/s", "GB/s", "hbm"
+            self.units = self.bytes / 1e9
+            self.kernel_file, self.kernel = "ln_fused.cu", "ln_fused"
+        self.dev_in = [t.to(dev) for t in self.host]
+        self._alloc_outputs()
+
+    def _alloc_outputs(self):
+        d, dev = self.w.dims, self.dev
+        if self.w.kind == "attn":
+            q = self.dev_in[0]
+            self.o = torch.empty_like(q)
+            self.lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+            self.outs = [self.o, self.lse]
+        elif self.w.kind == "decode":
+            q = self.dev_in[0]
+            self.ws = self.rf.decode_workspace(d["B"], d["Hq"], d["D"], d["splits"], dev)
+            self.o = torch.empty((d["B"], d["Hq"], d["D"]), dtype=q.dtype, device=dev)
+            self.lse = torch.empty((d["B"], d["Hq"]), dtype=torch.float32, device=dev)
+            self.outs = [self.o, self.lse]
+        else:
+            self.o = torch.empty_like(self.dev_in[0])
+            self.outs = [self.o]
+
+    def step(self, ins=None):
+        rf, d = self.rf, self.w.dims
+        ins = ins or self.dev_in
+        if self.w.kind == "attn":
+            rf.rf_attn_fwd(ins[0], ins[1], ins[2], self.o, self.lse, scale=self.scale, causal=bool(d["causal"]))
+        elif self.w.kind == "decode":
+            rf.rf_attn_decode_splitkv(ins[0], ins[1], ins[2], self.o, self.ws, d["splits"], lse=self.lse,
+                                      scale=self.scale)
+        else:
+            rf.rf_layernorm_fused(ins[0], ins[1], ins[2], ins[3], self.o, eps=d["eps"])
+
+    def describe(self):
+        d = dict(self.w.dims)
+        return {"workload": self.w.name, **d, "dtype": self.dtype, "seed": self.w.seed}
+
+
+def time_steps(runner, steps, warmup, flush):
+    """Per-step device time (ms) with events around the step only; L2 flushed before each step."""
+    for _ in range(warmup):
+        flush.zero_()
+        runner.step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record()
+        runner.step()
+        ends[i].record()
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def time_e2e(runner, steps, warmup):
+    """Same step through the public API with pinned host buffers: H2D of the inputs,
+    the call, D2H of the outputs, all inside the timed region."""
+    pinned_in = [t.pin_memory() for t in runner.host]
+    pinned_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in runner.outs]
+    dev_in = [torch.empty_like(t) for t in runner.dev_in]
+
+    def one():
+        for dst, src in zip(dev_in, pinned_in):
+            dst.copy_(src, non_blocking=True)
+        runner.step(dev_in)
+        for dst, src in zip(pinned_out, runner.outs):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        one()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    h2d = sum(t.numel() * t.element_size() for t in pinned_in)
+    d2h = sum(t.numel() * t.element_size() for t in pinned_out)
+    return ms, h2d, d2h
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_sample(w, host, budget_s=12.0):
+    """Time the fp64 oracle on a bounded sample of the workload; returns
+    (value in the workload's unit, sample description, seconds)."""
+    import oracle
+
+    d = w.dims
+    t_start = time.perf_counter()
+    done_units, what = 0.0, ""
+    if w.kind == "attn":
+        q, k, v = host
+        scale = float(np.float32(1.0 / math.sqrt(d["D"])))
+        G = d["Hq"] // d["Hkv"]
+        heads = 0
+        for b in range(d["B"]):
+            for h in range(d["Hq"]):
+                if heads and time.perf_counter() - t_start > budget_s:
+                    break
+                # a block of query rows of one head against all its keys
+                rows = min(d["N"], 1024 if d["N"] > 1024 else d["N"])
+                r0 = d["N"] - rows
+                oracle.attention(q[b:b + 1, h:h + 1, r0:], k[b:b + 1, h // G:h // G + 1],
+                                 v[b:b + 1, h // G:h // G + 1], scale, bool(d["causal"]))
+                vis = rows * d["N"] if not d["causal"] else sum(i + 1 for i in range(r0, d["N"]))
+                done_units += 4.0 * vis * d["D"] / 1e12
+                heads += 1
+        what = f"{heads} (batch, head) pairs x the last {rows} query rows against all keys"
+    elif w.kind == "decode":
+        q, k, v = host
+        scale = float(np.float32(1.0 / math.sqrt(d["D"])))
+        G = d["Hq"] // d["Hkv"]
+        groups = 0
+        for b in range(d["B"]):
+            for hk in range(d["Hkv"]):
+                if groups and time.perf_counter() - t_start > budget_s:
+                    break
+                oracle.decode(q[b:b + 1, hk * G:(hk + 1) * G], k[b:b + 1, hk:hk + 1], v[b:b + 1, hk:hk + 1], scale)
+                done_units += workmodel.decode_bytes(1, G, 1, d["L"], d["D"], w.dtype) / 1e9
+                groups += 1
+        what = f"{groups} (batch, kv-head) groups of {G} query heads over all {d['L']} keys"
+    else:
+        x, r, g, b = host
+        rows = 0
+        step = 512
+        while rows < d["rows"] and (rows == 0 or time.perf_counter() - t_start < budget_s):
+            oracle.layernorm(x[rows:rows + step], r[rows:rows + step], g, b, d["eps"])
+            rows += step
+        done_units = workmodel.layernorm_bytes(rows, d["cols"], w.dtype) / 1e9
+        what = f"the first {rows} of {d['rows']} rows"
+    secs = time.perf_counter() - t_start
+    return done_units / secs, what, secs
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+        return int(n)
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------- main
+def measure(name, dev, steps, warmup, flush, peaks, with_e2e=True):
+    r = Runner(name, dev)
+    times = time_steps(r, steps, warmup, flush)
+    ms = float(np.mean(times))
+    val = r.units / (ms / 1e3)
+    achieved_unit = "TFLOP/s" if r.bound == "tensor" else ("GB/s" if r.bound == "hbm" else "TFLOP/s")
+    if r.bound == "hbm":
+        achieved, peak = r.bytes / (ms / 1e3) / 1e9, peaks["hbm_gbs"]
+    elif r.bound == "tensor":
+        achieved, peak = r.flops / (ms / 1e3) / 1e12, peaks["bf16_tflops"]
+    else:  # fp32 FFMA: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz
+        achieved, peak = r.flops / (ms / 1e3) / 1e12, 152 * 128 * 2 * 2.07e9 / 1e12
+    res = {
+        "workload": name, "value": val, "unit": r.unit, "ms_per_step": ms,
+        "ms_p10": float(np.percentile(times, 10)), "ms_p90": float(np.percentile(times, 90)),
+        "roofline": {"bound": r.bound, "achieved": achieved, "peak": peak, "unit": achieved_unit,
+                     "frac": achieved / peak, "traffic": kernel_traffic(r.kernel_file, name),
+                     "kernel": r.kernel,
+                     "peak_source": peaks["source"] if r.bound != "alu" else "derived: 152 SMs x 128 FFMA x 2 x 2.07 GHz"},
+        "algorithmic_bytes": r.bytes, "algorithmic_flops": r.flops, "config": r.describe(),
+    }
+    if with_e2e:
+        e_ms, h2d, d2h = time_e2e(r, max(3, min(steps, 10)), 2)
+        res["e2e"] = {"value": r.units / (e_ms / 1e3), "unit": r.unit, "h2d_bytes_per_step": h2d,
+                      "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+    return r, res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="attn_fwd_f16_d64", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--no-parts", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = inputs.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        host = inputs.make(w)
+        per_step = []
+        for i in range(args.warmup + args.steps):
+            v, what, secs = oracle_sample(w, host, budget_s=max(0.5, 60.0 / (args.warmup + args.steps)))
+            if i >= args.warmup:
+                per_step.append((v, secs))
+        val = float(np.mean([v for v, _ in per_step]))
+        unit = "TFLOP/s" if w.kind == "attn" else "GB/s"
+        ms = float(np.mean([s for _, s in per_step]) * 1e3)
+        print(json.dumps({
+            "impl": "reference", "metric": "fused cascaded-reduction throughput (CPU fp64 oracle)", "value": val,
+            "unit": unit, "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, **w.dims, "input_dtype": w.dtype, "seed": w.seed},
+            "cpu_baseline": {"value": val, "unit": unit, "cores": cpu_threads(), "kind": "oracle", "sample": what},
+            "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return
+
+    import cascaded_reductions_pass_gb300 as rf
+
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    rf.load()
+    peaks = load_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    sampler = ClockSampler(local)
+    sampler.start()
+
+    # the headline workload: replicas on every rank, bracketed by barriers
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    runner, res = measure(args.workload, dev, args.steps, args.warmup, flush, peaks, with_e2e=False)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t1 = time.time()
+    total_ms = sum([res["ms_per_step"]]) * args.steps
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms = total_ms / args.steps
+    value = world * runner.units / (ms / 1e3)
+    e_ms, h2d, d2h = time_e2e(runner, max(3, min(args.steps, 10)), 3)
+    e2e_val = runner.units / (e_ms / 1e3)
+    if world > 1:
+        et = torch.tensor([e_ms], device=dev)
+        dist.all_reduce(et, op=dist.ReduceOp.MAX)
+        e2e_val = world * runner.units / (float(et.item()) / 1e3)
+    clocks = sampler.summary(t0, t1)
+    launches = args.steps * (2 if w.kind == "decode" else 1)
+
+    parts = {}
+    if not args.no_parts and rank == 0:
+        for name in inputs.WORKLOADS:
+            if name == args.workload:
+                continue
+            try:
+                _, pres = measure(name, dev, max(10, args.steps // 2), args.warmup, flush, peaks, with_e2e=True)
+                parts[name] = pres
+            except Exception as exc:  # a workload whose kernel is unavailable is reported, not hidden
+                parts[name] = {"error": f"{type(exc).__name__}: {exc}"}
+            torch.cuda.empty_cache()
+    sampler.stop()
+    status = rf.rf_device_status()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, what, secs = oracle_sample(w, runner.host, budget_s=15.0)
+        cpu = {"value": v, "unit": runner.unit, "cores": cpu_threads(), "kind": "oracle", "sample": what,
+               "seconds": secs}
+
+    if rank == 0:
+        line = {
+            "metric": runner.metric, "value": value, "unit": runner.unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": runner.dtype, "data": "synthetic",
+            "config": {**runner.describe(), "l2": "flushed before every step (512 MiB memset, outside the events)",
+                       "parallelism": f"replicas{world}" if world > 1 else "single-gpu"},
+            "roofline": res["roofline"],
+            "e2e": {"value": e2e_val, "unit": runner.unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e_ms},
+            "gpu_launches": launches, "clocks": clocks, "cpu_baseline": cpu,
+            "device_status": int(status), "parts": parts,
+            "ms_p10": res["ms_p10"], "ms_p90": res["ms_p90"],
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

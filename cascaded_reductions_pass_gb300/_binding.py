@@ -1,5 +1,236 @@
-"""ctypes binding of librf.so (placeholder until the C-ABI lands)."""
+"""ctypes binding of librf.so, the C ABI declared in include/rf.h.
+
+Argument marshalling only: each ``rf_*`` function here takes torch tensors
+that already live on the GPU, reads their shapes, pointers and dtype, and calls
+the C function of the same name.  Every step of the computation runs in the
+library's CUDA kernels.  There is no fallback: if librf.so is missing the
+first call raises, and a non-OK status raises ``RFError`` with the library's
+message.
+
+The ``attention``, ``decode`` and ``layernorm`` helpers additionally allocate
+the outputs (and the decode workspace) with torch before calling the C ABI.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "librf.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "rf.h")
+
+RF_OK, RF_ERR_INVALID_ARG, RF_ERR_UNSUPPORTED, RF_ERR_CUDA, RF_ERR_TIMEOUT = range(5)
+STATUS_NAMES = {0: "RF_OK", 1: "RF_ERR_INVALID_ARG", 2: "RF_ERR_UNSUPPORTED", 3: "RF_ERR_CUDA", 4: "RF_ERR_TIMEOUT"}
+DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+
+_lib = None
+
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_SIGNATURES = {
+    "rf_attn_fwd": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp], _i),
+    "rf_attn_decode_splitkv_workspace_bytes": ([_i, _i, _i, _i], _sz),
+    "rf_attn_decode_splitkv": ([_vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _i, _f, _i, _vp], _i),
+    "rf_lse_merge": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp], _i),
+    "rf_layernorm_fused": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _f, _i, _vp], _i),
+    "rf_last_error": ([], ctypes.c_char_p),
+    "rf_version": ([], _i),
+    "rf_device_status": ([_vp, _i], _i),
+}
 
 
-def load():
-    raise RuntimeError("librf.so not built")
+class RFError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def load(path: str | None = None):
+    """Load librf.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or os.environ.get("RF_LIBRARY") or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"librf.so not found at {path}: build it with "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    for name, (args, res) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def declared_symbols(header: str = HEADER):
+    """Names of the functions declared in include/rf.h."""
+    with open(header) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rf_[a-z0-9_]+)\s*\(", text)))
+
+
+def _check(status: int):
+    if status != RF_OK:
+        raise RFError(status, load().rf_last_error().decode())
+
+
+def _dev(t, name, nullable=False):
+    if t is None:
+        if nullable:
+            return None
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _code(dtype):
+    if dtype not in DTYPE_CODES:
+        raise ValueError(f"unsupported dtype {dtype}")
+    return DTYPE_CODES[dtype]
+
+
+def rf_version() -> int:
+    return load().rf_version()
+
+
+def rf_last_error() -> str:
+    return load().rf_last_error().decode()
+
+
+def rf_device_status(stream=None, clear=True) -> int:
+    """Synchronise the stream and return the device status (RF_OK or RF_ERR_TIMEOUT)."""
+    return load().rf_device_status(_stream(stream), int(bool(clear)))
+
+
+def rf_attn_fwd(q, k, v, o, lse=None, scale=None, causal=False, stream=None):
+    """o[B,Hq,Nq,D] (and lse[B,Hq,Nq] fp32) <- attention(q[B,Hq,Nq,D], k/v[B,Hkv,Nk,D])."""
+    B, Hq, Nq, D = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, Hkv, Nk, D) or tuple(v.shape) != tuple(k.shape) or tuple(o.shape) != tuple(q.shape):
+        raise ValueError("shape mismatch among q, k, v, o")
+    if not (q.dtype == k.dtype == v.dtype == o.dtype):
+        raise ValueError("q, k, v and o must share a dtype")
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, Nq)):
+        raise ValueError("lse must be float32 [B,Hq,Nq]")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check(load().rf_attn_fwd(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(o, "o"), _dev(lse, "lse", True),
+                              B, Hq, Hkv, Nq, Nk, D, scale, int(bool(causal)), _code(q.dtype), _stream(stream)))
+
+
+def rf_attn_decode_splitkv_workspace_bytes(B, Hq, D, num_splits) -> int:
+    return load().rf_attn_decode_splitkv_workspace_bytes(B, Hq, D, num_splits)
+
+
+def rf_attn_decode_splitkv(q, k_cache, v_cache, o, workspace, num_splits, lse=None, scale=None, stream=None):
+    """o[B,Hq,D] (and lse[B,Hq]) <- one-query attention over k/v_cache[B,Hkv,L,D], split in num_splits."""
+    if q.dim() == 4:
+        q = q.reshape(q.shape[0], q.shape[1], q.shape[3])
+    B, Hq, D = q.shape
+    Hkv, L = k_cache.shape[1], k_cache.shape[2]
+    if tuple(k_cache.shape) != (B, Hkv, L, D) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache / v_cache shape mismatch")
+    if o.numel() != B * Hq * D or o.dtype != q.dtype:
+        raise ValueError("o must hold B*Hq*D elements of q's dtype")
+    if lse is not None and (lse.dtype != torch.float32 or lse.numel() != B * Hq):
+        raise ValueError("lse must be float32 with B*Hq elements")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load().rf_attn_decode_splitkv(_dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+                                         _dev(o, "o"), _dev(lse, "lse", True), _dev(workspace, "workspace"),
+                                         ws_bytes, B, Hq, Hkv, L, D, int(num_splits), scale, _code(q.dtype),
+                                         _stream(stream)))
+
+
+def rf_lse_merge(o_part, lse_part, o, lse=None, stream=None):
+    """o[rows,D] (and lse[rows]) <- merge of o_part[rows,S,D], lse_part[rows,S] (fp32)."""
+    rows, S, D = o_part.shape
+    if o_part.dtype != torch.float32 or lse_part.dtype != torch.float32 or tuple(lse_part.shape) != (rows, S):
+        raise ValueError("o_part [rows,S,D] and lse_part [rows,S] must be float32")
+    if o.numel() != rows * D:
+        raise ValueError("o must hold rows*D elements")
+    if lse is not None and (lse.dtype != torch.float32 or lse.numel() != rows):
+        raise ValueError("lse must be float32 with rows elements")
+    _check(load().rf_lse_merge(_dev(o_part, "o_part"), _dev(lse_part, "lse_part"), _dev(o, "o"),
+                               _dev(lse, "lse", True), rows, S, D, _code(o.dtype), _stream(stream)))
+
+
+def rf_layernorm_fused(x, residual, gamma, beta, out, eps=1e-5, residual_out=None, stream=None):
+    """out[rows,cols] <- LayerNorm(x + residual) * gamma + beta (residual/gamma/beta/residual_out may be None)."""
+    rows, cols = x.shape
+    for name, t in (("residual", residual), ("out", out), ("residual_out", residual_out)):
+        if t is not None and (tuple(t.shape) != (rows, cols) or t.dtype != x.dtype):
+            raise ValueError(f"{name} must match x")
+    for name, t in (("gamma", gamma), ("beta", beta)):
+        if t is not None and (t.numel() != cols or t.dtype != x.dtype):
+            raise ValueError(f"{name} must hold cols elements of x's dtype")
+    _check(load().rf_layernorm_fused(_dev(x, "x"), _dev(residual, "residual", True), _dev(gamma, "gamma", True),
+                                     _dev(beta, "beta", True), _dev(out, "out"),
+                                     _dev(residual_out, "residual_out", True), rows, cols, float(eps),
+                                     _code(x.dtype), _stream(stream)))
+
+
+# ------------------------------------------------------------------ allocating helpers
+def attention(q, k, v, scale=None, causal=False, stream=None):
+    """Allocate (o, lse) and run rf_attn_fwd."""
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    rf_attn_fwd(q, k, v, o, lse, scale=scale, causal=causal, stream=stream)
+    return o, lse
+
+
+def decode_workspace(B, Hq, D, num_splits, device="cuda"):
+    n = rf_attn_decode_splitkv_workspace_bytes(B, Hq, D, num_splits)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def decode(q, k_cache, v_cache, num_splits, scale=None, workspace=None, stream=None):
+    """Allocate (o [B,Hq,D], lse [B,Hq]) and a workspace if none is given, then run rf_attn_decode_splitkv."""
+    B, Hq, D = q.shape[0], q.shape[1], q.shape[-1]
+    if workspace is None:
+        workspace = decode_workspace(B, Hq, D, num_splits, q.device)
+    o = torch.empty((B, Hq, D), dtype=q.dtype, device=q.device)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    rf_attn_decode_splitkv(q, k_cache, v_cache, o, workspace, num_splits, lse=lse, scale=scale, stream=stream)
+    return o, lse
+
+
+def decode_partials_view(workspace, B, Hq, D, num_splits):
+    """(o_part [B,Hq,S,D], lse_part [B,Hq,S]) views of a decode workspace."""
+    rows = B * Hq
+    o_bytes = (rows * num_splits * D * 4 + 255) // 256 * 256
+    o_part = workspace[: rows * num_splits * D * 4].view(torch.float32).view(B, Hq, num_splits, D)
+    lse_part = workspace[o_bytes: o_bytes + rows * num_splits * 4].view(torch.float32).view(B, Hq, num_splits)
+    return o_part, lse_part
+
+
+def layernorm(x, residual, gamma, beta, eps=1e-5, want_residual_out=False, stream=None):
+    out = torch.empty_like(x)
+    rout = torch.empty_like(x) if want_residual_out else None
+    rf_layernorm_fused(x, residual, gamma, beta, out, eps=eps, residual_out=rout, stream=stream)
+    return (out, rout) if want_residual_out else out
+
+
+__all__ = [
+    "RFError", "load", "declared_symbols", "rf_version", "rf_last_error", "rf_device_status", "rf_attn_fwd",
+    "rf_attn_decode_splitkv_workspace_bytes", "rf_attn_decode_splitkv", "rf_lse_merge", "rf_layernorm_fused",
+    "attention", "decode", "decode_workspace", "decode_partials_view", "layernorm",
+    "RF_OK", "RF_ERR_INVALID_ARG", "RF_ERR_UNSUPPORTED", "RF_ERR_CUDA", "RF_ERR_TIMEOUT",
+]

@@ -1,0 +1,150 @@
+// attn_fwd_f32.cu -- exact fp32 attention forward on the FP32 pipes (SIMT).
+//
+// The cascade max -> sum exp -> sum exp * v (RedFuser, Abstract: safe softmax
+// followed by GEMM) fused into one loop over key tiles in the incremental
+// form (RedFuser, Figure 4): for each tile of 32 keys the running row max m
+// (level 1, reduce max / combine +) is raised, the running sum l and the
+// running output acc (levels 2-3, reduce + / combine *) are rescaled by
+// exp(m_old - m_new) and the tile's terms are added.  O = acc / l and
+// LSE = m + ln l at the end.  fp32 tensor-core modes (TF32) round the
+// operands to 10 mantissa bits, too coarse for a 1e-5 relative result, so
+// this path uses FFMA throughout with the accurate expf/logf.
+//
+// CTA: 4 warps, 16 query rows (4 per warp), key tiles of 32 (one key per
+// lane) staged in shared memory with K rows padded to D+4 floats.
+#include <math.h>
+
+#include "rf_device.cuh"
+
+namespace rf {
+namespace {
+
+constexpr int kRowsPerWarp = 4;
+constexpr int kWarps = 4;
+constexpr int kBM = kRowsPerWarp * kWarps;  // 16 query rows per CTA
+constexpr int kBN = 32;                     // keys per tile
+
+template <int DC>  // DC = ceil(D / 32) output columns per lane
+__global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const float* __restrict__ q,
+                                                               const float* __restrict__ k,
+                                                               const float* __restrict__ v, float* __restrict__ o,
+                                                               float* __restrict__ lse, int Hq, int Hkv, int Nq,
+                                                               int Nk, int D, float scale, int causal) {
+  extern __shared__ float4 smem4[];
+  float* smem = reinterpret_cast<float*>(smem4);
+  const int KS = D + 4;               // padded K row stride (floats)
+  float* Qs = smem;                   // [kBM][D]
+  float* Ks = Qs + kBM * D;           // [kBN][KS]
+  float* Vs = Ks + kBN * KS;          // [kBN][D]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.z, h = blockIdx.y, hk = h / (Hq / Hkv);
+  const int q0 = blockIdx.x * kBM;
+  const float* qh = q + (static_cast<long long>(b) * Hq + h) * Nq * D;
+  const float* kh = k + (static_cast<long long>(b) * Hkv + hk) * Nk * D;
+  const float* vh = v + (static_cast<long long>(b) * Hkv + hk) * Nk * D;
+  const int D4 = D >> 2;
+
+  for (int i = threadIdx.x; i < kBM * D4; i += blockDim.x) {
+    const int r = i / D4, c = i - r * D4;
+    float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (q0 + r < Nq) val = reinterpret_cast<const float4*>(qh + static_cast<long long>(q0 + r) * D)[c];
+    reinterpret_cast<float4*>(Qs + r * D)[c] = val;
+  }
+
+  float m[kRowsPerWarp], l[kRowsPerWarp], acc[kRowsPerWarp][DC];
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    m[r] = -INFINITY;
+    l[r] = 0.f;
+#pragma unroll
+    for (int c = 0; c < DC; ++c) acc[r][c] = 0.f;
+  }
+
+  const int last_row = min(q0 + kBM, Nq) - 1;
+  const int kend = causal ? min(Nk, last_row + 1) : Nk;  // keys past the CTA's last row are all masked
+  for (int k0 = 0; k0 < kend; k0 += kBN) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < kBN * D4; i += blockDim.x) {
+      const int r = i / D4, c = i - r * D4;
+      float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
+      if (k0 + r < Nk) {
+        kv = reinterpret_cast<const float4*>(kh + static_cast<long long>(k0 + r) * D)[c];
+        vv = reinterpret_cast<const float4*>(vh + static_cast<long long>(k0 + r) * D)[c];
+      }
+      reinterpret_cast<float4*>(Ks + r * KS)[c] = kv;
+      reinterpret_cast<float4*>(Vs + r * D)[c] = vv;
+    }
+    __syncthreads();
+
+    const int key = k0 + lane;
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      const int qi = q0 + warp * kRowsPerWarp + r;
+      const float* qr = Qs + (warp * kRowsPerWarp + r) * D;
+      const float* kr = Ks + lane * KS;
+      float dot = 0.f;
+      for (int d = 0; d < D; d += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(qr + d);
+        const float4 c = *reinterpret_cast<const float4*>(kr + d);
+        dot = fmaf(a.x, c.x, dot);
+        dot = fmaf(a.y, c.y, dot);
+        dot = fmaf(a.z, c.z, dot);
+        dot = fmaf(a.w, c.w, dot);
+      }
+      const bool visible = key < Nk && (!causal || key <= qi);
+      const float s = visible ? dot * scale : -INFINITY;
+      const float m_new = fmaxf(m[r], warp_max(s));
+      if (m_new == -INFINITY) continue;  // no visible key for this row yet
+      const float alpha = expf(m[r] - m_new);  // 0 when m was -inf
+      const float p = expf(s - m_new);          // 0 for masked keys
+      l[r] = fmaf(l[r], alpha, warp_sum(p));
+#pragma unroll
+      for (int c = 0; c < DC; ++c) acc[r][c] *= alpha;
+      for (int j = 0; j < kBN; ++j) {
+        const float pj = __shfl_sync(0xffffffffu, p, j);
+        const float* vr = Vs + j * D;
+#pragma unroll
+        for (int c = 0; c < DC; ++c) {
+          const int d = lane + 32 * c;
+          if (d < D) acc[r][c] = fmaf(pj, vr[d], acc[r][c]);
+        }
+      }
+      m[r] = m_new;
+    }
+  }
+
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    const int qi = q0 + warp * kRowsPerWarp + r;
+    if (qi >= Nq) continue;
+    const long long orow = (static_cast<long long>(b) * Hq + h) * Nq + qi;
+    const bool live = l[r] > 0.f;
+    const float inv = live ? 1.0f / l[r] : 0.f;
+#pragma unroll
+    for (int c = 0; c < DC; ++c) {
+      const int d = lane + 32 * c;
+      if (d < D) o[orow * D + d] = acc[r][c] * inv;
+    }
+    if (lse && lane == 0) lse[orow] = live ? m[r] + logf(l[r]) : -INFINITY;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B, int Hq,
+                            int Hkv, int Nq, int Nk, int D, float scale, int causal, cudaStream_t s) {
+  const dim3 grid((Nq + kBM - 1) / kBM, Hq, B);
+  if (B > 65535 || Hq > 65535) return cudaErrorInvalidConfiguration;
+  const size_t smem = sizeof(float) * (kBM * D + kBN * (D + 4) + kBN * D);
+  const int dc = (D + 31) / 32;
+  switch (dc) {
+    case 1: attn_f32_kernel<1><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal); break;
+    case 2: attn_f32_kernel<2><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal); break;
+    case 3: attn_f32_kernel<3><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal); break;
+    default: attn_f32_kernel<4><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal); break;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace rf

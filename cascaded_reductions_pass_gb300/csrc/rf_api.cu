@@ -1,0 +1,315 @@
+// rf_api.cu -- the C ABI of librf.so (declared in include/rf.h).
+//
+// Host code only: argument validation, kernel selection and launch.  Every
+// check runs before anything is enqueued; a failing check returns a status and
+// records a message for rf_last_error().  The device-side status word that
+// kernels set when a bounded wait runs out lives here.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "rf.h"
+#include "rf_internal.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+rf_status_t fail(rf_status_t st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+const char* dt_name(rf_dtype_t d) {
+  switch (d) {
+    case RF_F32: return "f32";
+    case RF_F16: return "f16";
+    case RF_BF16: return "bf16";
+  }
+  return "?";
+}
+
+bool valid_dtype(rf_dtype_t d) { return d == RF_F32 || d == RF_F16 || d == RF_BF16; }
+
+// Rejects pointers the current device cannot use as device memory (host or
+// unregistered memory, or another device's memory).  Runs after the pure host
+// checks, so argument errors are reported without touching CUDA.
+rf_status_t check_dev_ptr(const void* p, const char* name) {
+  if (p == nullptr) return RF_OK;
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(RF_ERR_INVALID_ARG, "%s: cannot query pointer (%s)", name, cudaGetErrorString(e));
+  }
+  if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
+    return fail(RF_ERR_INVALID_ARG, "%s is not device memory (pass a device pointer)", name);
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(RF_ERR_CUDA, "cudaGetDevice failed");
+  }
+  if (a.type == cudaMemoryTypeDevice && a.device != dev)
+    return fail(RF_ERR_INVALID_ARG, "%s lives on device %d, current device is %d", name, a.device, dev);
+  return RF_OK;
+}
+
+#define RF_TRY(expr)                   \
+  do {                                 \
+    rf_status_t _st = (expr);          \
+    if (_st != RF_OK) return _st;      \
+  } while (0)
+
+rf_status_t launched(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(RF_ERR_CUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
+  }
+  g_last_error[0] = '\0';
+  return RF_OK;
+}
+
+size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+
+}  // namespace
+
+// Device status word: set (atomicOr) by a kernel whose bounded wait ran out.
+__device__ unsigned int g_rf_status;
+
+namespace rf {
+
+unsigned* device_status_ptr() {
+  static std::mutex mu;
+  static unsigned* ptrs[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_rf_status) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    ptrs[dev] = static_cast<unsigned*>(p);
+  }
+  return ptrs[dev];
+}
+
+bool encode_tma_3d_16bit(void* tmap_out, const void* base, uint64_t inner, uint64_t rows,
+                         uint64_t outer, uint32_t box_rows, cudaError_t* err) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    else
+      cudaGetLastError();
+  });
+  if (encode == nullptr) {
+    *err = cudaErrorNotSupported;
+    return false;
+  }
+  cuuint64_t dims[3] = {inner, rows, outer};
+  cuuint64_t strides[2] = {inner * 2, inner * 2 * rows};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(reinterpret_cast<CUtensorMap*>(tmap_out), CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
+                      const_cast<void*>(base), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    *err = cudaErrorInvalidValue;
+    return false;
+  }
+  return true;
+}
+
+}  // namespace rf
+
+extern "C" {
+
+const char* rf_last_error(void) { return g_last_error; }
+
+int rf_version(void) { return RF_VERSION; }
+
+rf_status_t rf_device_status(void* stream, int clear) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(RF_ERR_CUDA, "stream synchronise failed: %s", cudaGetErrorString(e));
+  }
+  unsigned v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_rf_status, sizeof(v));
+  if (e == cudaSuccess && clear) {
+    unsigned z = 0;
+    e = cudaMemcpyToSymbol(g_rf_status, &z, sizeof(z));
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(RF_ERR_CUDA, "status word access failed: %s", cudaGetErrorString(e));
+  }
+  if (v != 0) return fail(RF_ERR_TIMEOUT, "a device-side bounded wait ran out (code 0x%x)", v);
+  g_last_error[0] = '\0';
+  return RF_OK;
+}
+
+rf_status_t rf_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal,
+                        rf_dtype_t dtype, void* stream) {
+  if (!q || !k || !v || !o) return fail(RF_ERR_INVALID_ARG, "rf_attn_fwd: q, k, v and o must be non-null");
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || D <= 0)
+    return fail(RF_ERR_INVALID_ARG, "rf_attn_fwd: sizes must be positive (B=%d Hq=%d Hkv=%d Nq=%d Nk=%d D=%d)",
+                B, Hq, Hkv, Nq, Nk, D);
+  if (Hq % Hkv != 0) return fail(RF_ERR_INVALID_ARG, "rf_attn_fwd: Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
+  if (!(scale > 0.0f) || !std::isfinite(scale))
+    return fail(RF_ERR_INVALID_ARG, "rf_attn_fwd: scale must be finite and positive");
+  if (!valid_dtype(dtype)) return fail(RF_ERR_INVALID_ARG, "rf_attn_fwd: unknown dtype %d", int(dtype));
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return fail(RF_ERR_INVALID_ARG, "rf_attn_fwd: pointers must be 16-byte aligned");
+  if (causal && Nq != Nk)
+    return fail(RF_ERR_UNSUPPORTED, "rf_attn_fwd: causal mask requires Nq == Nk (got %d, %d)", Nq, Nk);
+  if (dtype == RF_F32) {
+    if (D % 4 != 0 || D > 128)
+      return fail(RF_ERR_UNSUPPORTED, "rf_attn_fwd: f32 path needs D %% 4 == 0 and D <= 128 (D=%d)", D);
+  } else if (D != 64 && D != 128) {
+    return fail(RF_ERR_UNSUPPORTED, "rf_attn_fwd: %s path supports D in {64, 128} (D=%d)", dt_name(dtype), D);
+  }
+  RF_TRY(check_dev_ptr(q, "q"));
+  RF_TRY(check_dev_ptr(k, "k"));
+  RF_TRY(check_dev_ptr(v, "v"));
+  RF_TRY(check_dev_ptr(o, "o"));
+  RF_TRY(check_dev_ptr(lse, "lse"));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == RF_F32)
+    return launched(rf::launch_attn_f32(static_cast<const float*>(q), static_cast<const float*>(k),
+                                        static_cast<const float*>(v), static_cast<float*>(o), lse, B, Hq,
+                                        Hkv, Nq, Nk, D, scale, causal, s),
+                    "rf_attn_fwd(f32)");
+  unsigned* st = rf::device_status_ptr();
+  if (!st) return fail(RF_ERR_CUDA, "rf_attn_fwd: cannot resolve the device status word");
+  return launched(rf::launch_attn_tc(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal,
+                                     static_cast<rf::Dt>(dtype), st, s),
+                  "rf_attn_fwd(tcgen05)");
+}
+
+size_t rf_attn_decode_splitkv_workspace_bytes(int B, int Hq, int D, int num_splits) {
+  if (B <= 0 || Hq <= 0 || D <= 0 || num_splits <= 0) return 0;
+  size_t rows = size_t(B) * size_t(Hq);
+  return align256(rows * size_t(num_splits) * size_t(D) * 4) + rows * size_t(num_splits) * 4;
+}
+
+rf_status_t rf_attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, void* o,
+                                   float* lse, void* workspace, size_t workspace_bytes, int B, int Hq,
+                                   int Hkv, int L, int D, int num_splits, float scale,
+                                   rf_dtype_t dtype, void* stream) {
+  if (!q || !k_cache || !v_cache || !o || !workspace)
+    return fail(RF_ERR_INVALID_ARG, "rf_attn_decode_splitkv: q, k_cache, v_cache, o and workspace must be non-null");
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || L <= 0 || D <= 0 || num_splits <= 0)
+    return fail(RF_ERR_INVALID_ARG, "rf_attn_decode_splitkv: sizes must be positive");
+  if (Hq % Hkv != 0)
+    return fail(RF_ERR_INVALID_ARG, "rf_attn_decode_splitkv: Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
+  if (!(scale > 0.0f) || !std::isfinite(scale))
+    return fail(RF_ERR_INVALID_ARG, "rf_attn_decode_splitkv: scale must be finite and positive");
+  if (!valid_dtype(dtype)) return fail(RF_ERR_INVALID_ARG, "rf_attn_decode_splitkv: unknown dtype %d", int(dtype));
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(lse))
+    return fail(RF_ERR_INVALID_ARG, "rf_attn_decode_splitkv: pointers must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(RF_ERR_INVALID_ARG, "rf_attn_decode_splitkv: workspace must be 256-byte aligned");
+  size_t need = rf_attn_decode_splitkv_workspace_bytes(B, Hq, D, num_splits);
+  if (workspace_bytes < need)
+    return fail(RF_ERR_INVALID_ARG, "rf_attn_decode_splitkv: workspace too small (%zu < %zu bytes)",
+                workspace_bytes, need);
+  if (dtype == RF_F32) return fail(RF_ERR_UNSUPPORTED, "rf_attn_decode_splitkv: f32 is not supported");
+  if (D != 64 && D != 128)
+    return fail(RF_ERR_UNSUPPORTED, "rf_attn_decode_splitkv: D must be 64 or 128 (D=%d)", D);
+  if (Hq / Hkv > 8)
+    return fail(RF_ERR_UNSUPPORTED, "rf_attn_decode_splitkv: at most 8 query heads per kv head (got %d)", Hq / Hkv);
+  if (num_splits > 256)
+    return fail(RF_ERR_UNSUPPORTED, "rf_attn_decode_splitkv: num_splits must be <= 256 (got %d)", num_splits);
+  RF_TRY(check_dev_ptr(q, "q"));
+  RF_TRY(check_dev_ptr(k_cache, "k_cache"));
+  RF_TRY(check_dev_ptr(v_cache, "v_cache"));
+  RF_TRY(check_dev_ptr(o, "o"));
+  RF_TRY(check_dev_ptr(lse, "lse"));
+  RF_TRY(check_dev_ptr(workspace, "workspace"));
+  unsigned* st = rf::device_status_ptr();
+  if (!st) return fail(RF_ERR_CUDA, "rf_attn_decode_splitkv: cannot resolve the device status word");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  size_t rows = size_t(B) * size_t(Hq);
+  float* o_part = static_cast<float*>(workspace);
+  float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                             align256(rows * size_t(num_splits) * size_t(D) * 4));
+  rf_status_t r = launched(rf::launch_decode_split(q, k_cache, v_cache, o_part, lse_part, B, Hq, Hkv, L,
+                                                   D, num_splits, scale, static_cast<rf::Dt>(dtype), st, s),
+                           "rf_attn_decode_splitkv(split)");
+  if (r != RF_OK) return r;
+  return launched(rf::launch_lse_merge(o_part, lse_part, o, lse, int(rows), num_splits, D,
+                                       static_cast<rf::Dt>(dtype), s),
+                  "rf_attn_decode_splitkv(merge)");
+}
+
+rf_status_t rf_lse_merge(const float* o_part, const float* lse_part, void* o, float* lse, int rows,
+                         int num_splits, int D, rf_dtype_t out_dtype, void* stream) {
+  if (!o_part || !lse_part || !o) return fail(RF_ERR_INVALID_ARG, "rf_lse_merge: o_part, lse_part and o must be non-null");
+  if (rows <= 0 || num_splits <= 0 || D <= 0)
+    return fail(RF_ERR_INVALID_ARG, "rf_lse_merge: sizes must be positive");
+  if (!valid_dtype(out_dtype)) return fail(RF_ERR_INVALID_ARG, "rf_lse_merge: unknown dtype %d", int(out_dtype));
+  if (!aligned16(o_part) || !aligned16(o))
+    return fail(RF_ERR_INVALID_ARG, "rf_lse_merge: o_part and o must be 16-byte aligned");
+  if (D % 4 != 0 || D > 512) return fail(RF_ERR_UNSUPPORTED, "rf_lse_merge: D must be a multiple of 4, <= 512");
+  if (num_splits > 256) return fail(RF_ERR_UNSUPPORTED, "rf_lse_merge: num_splits must be <= 256");
+  RF_TRY(check_dev_ptr(o_part, "o_part"));
+  RF_TRY(check_dev_ptr(lse_part, "lse_part"));
+  RF_TRY(check_dev_ptr(o, "o"));
+  RF_TRY(check_dev_ptr(lse, "lse"));
+  return launched(rf::launch_lse_merge(o_part, lse_part, o, lse, rows, num_splits, D,
+                                       static_cast<rf::Dt>(out_dtype), static_cast<cudaStream_t>(stream)),
+                  "rf_lse_merge");
+}
+
+rf_status_t rf_layernorm_fused(const void* x, const void* residual, const void* gamma, const void* beta,
+                               void* out, void* residual_out, int rows, int cols, float eps,
+                               rf_dtype_t dtype, void* stream) {
+  if (!x || !out) return fail(RF_ERR_INVALID_ARG, "rf_layernorm_fused: x and out must be non-null");
+  if (rows <= 0 || cols <= 0) return fail(RF_ERR_INVALID_ARG, "rf_layernorm_fused: sizes must be positive");
+  if (!(eps >= 0.0f) || !std::isfinite(eps))
+    return fail(RF_ERR_INVALID_ARG, "rf_layernorm_fused: eps must be finite and >= 0");
+  if (!valid_dtype(dtype)) return fail(RF_ERR_INVALID_ARG, "rf_layernorm_fused: unknown dtype %d", int(dtype));
+  if (!aligned16(x) || !aligned16(residual) || !aligned16(gamma) || !aligned16(beta) || !aligned16(out) ||
+      !aligned16(residual_out))
+    return fail(RF_ERR_INVALID_ARG, "rf_layernorm_fused: pointers must be 16-byte aligned");
+  int vec = dtype == RF_F32 ? 4 : 8;
+  if (cols % vec != 0)
+    return fail(RF_ERR_INVALID_ARG, "rf_layernorm_fused: cols=%d must be a multiple of %d for %s", cols, vec,
+                dt_name(dtype));
+  if (cols > rf::layernorm_max_cols(static_cast<rf::Dt>(dtype)))
+    return fail(RF_ERR_UNSUPPORTED, "rf_layernorm_fused: cols=%d exceeds %d", cols,
+                rf::layernorm_max_cols(static_cast<rf::Dt>(dtype)));
+  RF_TRY(check_dev_ptr(x, "x"));
+  RF_TRY(check_dev_ptr(residual, "residual"));
+  RF_TRY(check_dev_ptr(gamma, "gamma"));
+  RF_TRY(check_dev_ptr(beta, "beta"));
+  RF_TRY(check_dev_ptr(out, "out"));
+  RF_TRY(check_dev_ptr(residual_out, "residual_out"));
+  return launched(rf::launch_layernorm(x, residual, gamma, beta, out, residual_out, rows, cols, eps,
+                                       static_cast<rf::Dt>(dtype), static_cast<cudaStream_t>(stream)),
+                  "rf_layernorm_fused");
+}
+
+}  // extern "C"

@@ -1,0 +1,46 @@
+// Host-side declarations shared by the ABI front end (rf_api.cu) and the
+// kernel translation units.  Every launcher enqueues on `stream`, performs no
+// allocation and returns the launch's cudaError_t.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace rf {
+
+enum class Dt : int { F32 = 0, F16 = 1, BF16 = 2 };
+
+// residual + LayerNorm (ln_fused.cu)
+int layernorm_max_cols(Dt dt);
+cudaError_t launch_layernorm(const void* x, const void* r, const void* gamma, const void* beta,
+                             void* out, void* r_out, int rows, int cols, float eps, Dt dt,
+                             cudaStream_t s);
+
+// log-sum-exp merge of split partials (lse_merge.cu)
+cudaError_t launch_lse_merge(const float* o_part, const float* lse_part, void* o, float* lse,
+                             int rows, int splits, int D, Dt out_dt, cudaStream_t s);
+
+// exact fp32 SIMT attention forward (attn_fwd_f32.cu)
+cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, float* o, float* lse,
+                            int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal,
+                            cudaStream_t s);
+
+// split-KV decode partials (decode_split.cu): writes o_part [B*Hq, S, D] and
+// lse_part [B*Hq, S] fp32.
+cudaError_t launch_decode_split(const void* q, const void* k, const void* v, float* o_part,
+                                float* lse_part, int B, int Hq, int Hkv, int L, int D, int splits,
+                                float scale, Dt dt, unsigned* status, cudaStream_t s);
+
+// tcgen05 / TMEM / TMA attention forward for 16-bit inputs (attn_fwd_tc.cu)
+cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal,
+                           Dt dt, unsigned* status, cudaStream_t s);
+
+// TMA descriptor encoding through the driver entry point (rf_api.cu).
+// 3-D tensor [outer][rows][inner] of 16-bit elements, box {64, box_rows, 1},
+// 128-byte swizzle; returns false (and sets *err) on failure.
+bool encode_tma_3d_16bit(void* tmap_out, const void* base, uint64_t inner, uint64_t rows,
+                         uint64_t outer, uint32_t box_rows, cudaError_t* err);
+
+}  // namespace rf

@@ -1,0 +1,191 @@
+/*
+ * rf.h -- C ABI of librf.so: fused cascaded reductions on one GB300 (sm_103a).
+ *
+ * A cascaded reduction is a chain of reductions over one input stream where
+ * each level depends on the results of the levels before it (RedFuser: An
+ * Automatic Operator Fusion Framework for Cascaded Reductions on AI
+ * Accelerators, Abstract; Figures 1-2).  Every call below evaluates such a
+ * chain in one pass over its input, in the incremental form of RedFuser's
+ * Figure 4: as each block of input arrives, every level's running result is
+ * updated and the earlier levels' results are corrected with the combine
+ * operator that distributes over the reduce operator (RedFuser, Table 1:
+ * max with +, + with *).  The input is read from HBM once and the on-chip
+ * state has a constant size.
+ *
+ * Conventions shared by all calls
+ * -------------------------------
+ * - Every tensor pointer is a DEVICE pointer owned by the caller, contiguous
+ *   row-major in the layout stated at each call.  The library allocates no
+ *   device memory; the one call that needs scratch takes it from the caller
+ *   (rf_attn_decode_splitkv's workspace).
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream).  Calls are asynchronous: they enqueue kernels on `stream` and
+ *   return; results are ready once the stream has been synchronised.
+ * - `dtype` names the element type of the 16/32-bit tensors; accumulation is
+ *   always fp32.  Softmax scores use natural exponentials; LSE outputs are
+ *   natural logarithms of sum_j exp(scale * q.k_j).
+ * - Argument checks run on the host before anything is enqueued.  A failing
+ *   check returns an error status, leaves every output untouched and records a
+ *   message that rf_last_error() returns (per host thread).  No call aborts the
+ *   process, and no kernel traps: a device-side wait that runs out of its
+ *   iteration budget records RF_ERR_TIMEOUT in a device status word that
+ *   rf_device_status() reports.
+ */
+#ifndef RF_H_
+#define RF_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RF_VERSION 10000 /* 1.0.0 */
+
+typedef enum {
+  RF_OK = 0,
+  RF_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misalignment, short workspace */
+  RF_ERR_UNSUPPORTED = 2,  /* well-formed but not implemented (e.g. head dim) */
+  RF_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
+  RF_ERR_TIMEOUT = 4       /* a bounded device-side wait ran out (rf_device_status) */
+} rf_status_t;
+
+typedef enum { RF_F32 = 0, RF_F16 = 1, RF_BF16 = 2 } rf_dtype_t;
+
+/*
+ * rf_attn_fwd -- attention forward, the cascade max -> sum exp -> sum exp*v.
+ *
+ * Defines O = softmax(scale * Q K^T + mask) V per (batch, query head), the
+ * "safe softmax followed by GEMM" of RedFuser's Abstract and the attention
+ * fusion pattern of the "Operator Fusion" guide (section 2, Pattern 4), with
+ * level 1 the running row max, level 2 the running sum of exp(s - max) and
+ * level 3 the running exp-weighted sum of V, each rescaled by
+ * exp(max_old - max_new) when a key block raises the max.
+ *
+ *   q    [B, Hq,  Nq, D]  dtype          (read)
+ *   k, v [B, Hkv, Nk, D]  dtype          (read)
+ *   o    [B, Hq,  Nq, D]  dtype          (written)
+ *   lse  [B, Hq,  Nq]     fp32, nullable (written: max + ln(sum exp), natural log)
+ *   Query head h reads key/value head h / (Hq / Hkv) (grouped-query attention
+ *   with consecutive groups).  causal != 0 applies the top-left lower-triangular
+ *   mask (key j visible to query i iff j <= i) and requires Nq == Nk.
+ *
+ * Supported: dtype RF_F16 / RF_BF16 with D in {64, 128} (tcgen05 tensor-core
+ * kernel); dtype RF_F32 with D a multiple of 4, 4 <= D <= 128 (exact fp32 SIMT
+ * kernel).  Pointers must be 16-byte aligned.
+ * Errors: RF_ERR_INVALID_ARG for null q/k/v/o, B/Hq/Hkv/Nq/Nk/D <= 0,
+ * Hq % Hkv != 0, misalignment or a non-finite/non-positive scale;
+ * RF_ERR_UNSUPPORTED for other D, or causal with Nq != Nk; RF_ERR_CUDA if the
+ * launch fails.
+ */
+rf_status_t rf_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                        int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale,
+                        int causal, rf_dtype_t dtype, void* stream);
+
+/*
+ * rf_attn_decode_splitkv_workspace_bytes -- scratch size for rf_attn_decode_splitkv:
+ * fp32 partial outputs [B*Hq, num_splits, D] followed (at a 256-byte aligned
+ * offset) by fp32 partial LSEs [B*Hq, num_splits].  Returns 0 for non-positive
+ * arguments.
+ */
+size_t rf_attn_decode_splitkv_workspace_bytes(int B, int Hq, int D, int num_splits);
+
+/*
+ * rf_attn_decode_splitkv -- one decoding step (one query per head) over a KV
+ * cache, split along the keys and merged by log-sum-exp (split-KV or "flash"
+ * decoding: RedFuser, Figure 13 "FlashDecoding IR"; AttnFuse, Table 8).
+ *
+ * Split s covers the contiguous keys [floor(s*L/S), floor((s+1)*L/S)).  For
+ * each (batch, kv head, split) one CTA runs the fused cascade for all
+ * G = Hq/Hkv query heads of the group and writes the split's normalised O_s
+ * and lse_s into the workspace; a second kernel on the same stream merges the
+ * splits (the same combine as rf_lse_merge).  An empty split (L < S) has
+ * lse_s = -inf and weight 0.
+ *
+ *   q        [B, Hq, D]        dtype  (read; one query per head)
+ *   k_cache  [B, Hkv, L, D]    dtype  (read)
+ *   v_cache  [B, Hkv, L, D]    dtype  (read)
+ *   o        [B, Hq, D]        dtype  (written)
+ *   lse      [B, Hq]           fp32, nullable (written)
+ *   workspace: device scratch of at least
+ *     rf_attn_decode_splitkv_workspace_bytes(B, Hq, D, num_splits) bytes,
+ *     256-byte aligned, caller-owned; its contents after the call are the
+ *     per-split partials (layout as documented at the size query).
+ *
+ * Supported: dtype RF_F16 / RF_BF16, D in {64, 128}, 1 <= Hq/Hkv <= 8,
+ * 1 <= num_splits <= 256.  Pointers 16-byte aligned.
+ * Errors: RF_ERR_INVALID_ARG for null pointers, non-positive sizes,
+ * Hq % Hkv != 0, misalignment, or a short workspace; RF_ERR_UNSUPPORTED for
+ * other dtype / D / group size; RF_ERR_CUDA if a launch fails.
+ */
+rf_status_t rf_attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
+                                   void* o, float* lse, void* workspace, size_t workspace_bytes,
+                                   int B, int Hq, int Hkv, int L, int D, int num_splits,
+                                   float scale, rf_dtype_t dtype, void* stream);
+
+/*
+ * rf_lse_merge -- combine partial attention results computed over disjoint
+ * key sets: LSE = ln sum_s exp(lse_s), O = sum_s exp(lse_s - LSE) * O_s.
+ * This is the incremental combine across splits (RedFuser, Figure 4 and
+ * Figure 13): level 2 (sum, combine *) rebuilt from the parts' LSEs, level 3
+ * rescaled by the same weights.
+ *
+ *   o_part   [rows, num_splits, D] fp32 (read; normalised partial outputs)
+ *   lse_part [rows, num_splits]    fp32 (read; -inf marks an empty part)
+ *   o        [rows, D]             out_dtype (written)
+ *   lse      [rows]                fp32, nullable (written)
+ *   A row whose parts are all empty gets O = 0 and LSE = -inf.
+ *
+ * Supported: out_dtype RF_F32 / RF_F16 / RF_BF16, D a multiple of 4 up to 512,
+ * 1 <= num_splits <= 256.  o_part and o 16-byte aligned.
+ * Errors: RF_ERR_INVALID_ARG for null inputs/outputs, non-positive sizes or
+ * misalignment; RF_ERR_UNSUPPORTED for D or num_splits out of range;
+ * RF_ERR_CUDA if the launch fails.
+ */
+rf_status_t rf_lse_merge(const float* o_part, const float* lse_part, void* o, float* lse,
+                         int rows, int num_splits, int D, rf_dtype_t out_dtype, void* stream);
+
+/*
+ * rf_layernorm_fused -- residual add + LayerNorm in one pass over each row:
+ * h = x + residual; mean and biased variance of h (running count / mean / M2
+ * updated per element and merged across threads with the pairwise combine);
+ * y = (h - mean) / sqrt(var + eps) * gamma + beta ("Operator Fusion" guide,
+ * section 1 and section 2 Pattern 2; section 4 places eps inside the root).
+ * The row is kept on chip between the statistics and the normalisation, so
+ * x and residual are read once and y written once.
+ *
+ *   x, residual   [rows, cols] dtype (read; residual nullable = no residual add)
+ *   gamma, beta   [cols]       dtype (read; nullable = 1 and 0)
+ *   out           [rows, cols] dtype (written)
+ *   residual_out  [rows, cols] dtype, nullable (written: h rounded to dtype)
+ *
+ * Supported: dtype RF_F32 / RF_F16 / RF_BF16; cols a multiple of 16 bytes'
+ * worth of elements (8 for 16-bit, 4 for fp32) and at most 32768 (16-bit) or
+ * 16384 (fp32); all pointers 16-byte aligned.
+ * Errors: RF_ERR_INVALID_ARG for null x/out, non-positive sizes, eps < 0 or
+ * misalignment; RF_ERR_UNSUPPORTED for cols out of range; RF_ERR_CUDA if the
+ * launch fails.
+ */
+rf_status_t rf_layernorm_fused(const void* x, const void* residual, const void* gamma,
+                               const void* beta, void* out, void* residual_out,
+                               int rows, int cols, float eps, rf_dtype_t dtype, void* stream);
+
+/* Message for the last non-OK status returned on this host thread ("" if none). */
+const char* rf_last_error(void);
+
+/* RF_VERSION of the loaded library. */
+int rf_version(void);
+
+/*
+ * rf_device_status -- synchronise `stream`, then report whether any kernel of
+ * this library on the current device recorded a bounded wait that ran out
+ * (RF_ERR_TIMEOUT) since the status was last cleared; clear != 0 resets it.
+ * Returns RF_ERR_CUDA if the synchronisation itself fails.
+ */
+rf_status_t rf_device_status(void* stream, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RF_H_ */

@@ -1,0 +1,56 @@
+"""Comparison helpers for GPU-vs-oracle parity tests.
+
+Tolerances (stated once, used everywhere):
+* 16-bit outputs (fp16 / bf16): max |gpu - ref| <= 2e-2 AND
+  ||gpu - ref||_2 / ||ref||_2 <= 5e-3.
+* fp32 outputs: ||gpu - ref||_2 / ||ref||_2 <= 1e-5 AND
+  max |gpu - ref| / max |ref| <= 1e-5.
+* LSE (fp32, natural log): max abs error <= 1e-3 on 16-bit paths; on the fp32
+  path <= 1e-5 * max(1, max |ref|).
+"""
+import numpy as np
+import torch
+
+
+def to64(t):
+    if isinstance(t, torch.Tensor):
+        return t.detach().float().cpu().numpy().astype(np.float64)
+    return np.asarray(t, dtype=np.float64)
+
+
+def rel_l2(out, ref):
+    out, ref = to64(out), to64(ref)
+    den = np.linalg.norm(ref)
+    return float(np.linalg.norm(out - ref) / den) if den > 0 else float(np.linalg.norm(out))
+
+
+def max_abs(out, ref):
+    out, ref = to64(out), to64(ref)
+    return float(np.abs(out - ref).max()) if out.size else 0.0
+
+
+def check16(out, ref, what=""):
+    out, ref = to64(out), to64(ref)
+    assert out.shape == ref.shape, (out.shape, ref.shape)
+    assert np.isfinite(out).all(), f"{what}: non-finite output"
+    ma, rl = max_abs(out, ref), rel_l2(out, ref)
+    assert ma <= 2e-2 and rl <= 5e-3, f"{what}: max_abs={ma:.3e} rel_l2={rl:.3e}"
+    return ma, rl
+
+
+def check32(out, ref, what=""):
+    out, ref = to64(out), to64(ref)
+    assert out.shape == ref.shape, (out.shape, ref.shape)
+    rl = rel_l2(out, ref)
+    mr = max_abs(out, ref) / max(float(np.abs(ref).max()), 1e-300)
+    assert rl <= 1e-5 and mr <= 1e-5, f"{what}: rel_l2={rl:.3e} max_rel={mr:.3e}"
+    return rl, mr
+
+
+def check_lse(out, ref, tol=1e-3, what=""):
+    out, ref = to64(out), to64(ref)
+    fin = np.isfinite(ref)
+    assert (np.isneginf(out) == np.isneginf(ref)).all(), f"{what}: -inf pattern differs"
+    err = float(np.abs(out[fin] - ref[fin]).max()) if fin.any() else 0.0
+    assert err <= tol, f"{what}: lse max_abs={err:.3e}"
+    return err

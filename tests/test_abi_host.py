@@ -1,0 +1,134 @@
+"""The C ABI on the host, without a GPU: librf.so loads, exports every function
+that include/rf.h declares, and rejects bad arguments before touching CUDA."""
+import ctypes
+import subprocess
+
+import pytest
+
+import cascaded_reductions_pass_gb300 as rf
+from cascaded_reductions_pass_gb300 import _binding
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from cascaded_reductions_pass_gb300 import _build
+
+    _build.build()
+    return rf.load()
+
+
+def test_header_declares_the_four_calls():
+    names = rf.declared_symbols()
+    for n in ("rf_attn_fwd", "rf_attn_decode_splitkv", "rf_lse_merge", "rf_layernorm_fused",
+              "rf_attn_decode_splitkv_workspace_bytes", "rf_last_error", "rf_version", "rf_device_status"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", _binding.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for name in rf.declared_symbols():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_version(lib):
+    assert lib.rf_version() == 10000
+
+
+P = ctypes.c_void_p(0x10000)  # aligned, never dereferenced: every case below fails a host check first
+MIS = ctypes.c_void_p(0x10004)
+S = ctypes.c_void_p(0)
+
+
+def attn(lib, q=P, k=P, v=P, o=P, lse=None, B=1, Hq=2, Hkv=1, Nq=8, Nk=8, D=64, scale=0.125, causal=0, dt=1):
+    return lib.rf_attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dt, S)
+
+
+@pytest.mark.parametrize("kw,status,msg", [
+    (dict(q=None), rf.RF_ERR_INVALID_ARG, "non-null"),
+    (dict(o=None), rf.RF_ERR_INVALID_ARG, "non-null"),
+    (dict(B=0), rf.RF_ERR_INVALID_ARG, "positive"),
+    (dict(Nk=-1), rf.RF_ERR_INVALID_ARG, "positive"),
+    (dict(Hq=3, Hkv=2), rf.RF_ERR_INVALID_ARG, "multiple"),
+    (dict(scale=0.0), rf.RF_ERR_INVALID_ARG, "scale"),
+    (dict(scale=float("nan")), rf.RF_ERR_INVALID_ARG, "scale"),
+    (dict(dt=7), rf.RF_ERR_INVALID_ARG, "dtype"),
+    (dict(k=MIS), rf.RF_ERR_INVALID_ARG, "aligned"),
+    (dict(causal=1, Nq=8, Nk=9), rf.RF_ERR_UNSUPPORTED, "Nq == Nk"),
+    (dict(D=96), rf.RF_ERR_UNSUPPORTED, "D in {64, 128}"),
+    (dict(D=130, dt=0), rf.RF_ERR_UNSUPPORTED, "f32 path"),
+    (dict(D=6, dt=0), rf.RF_ERR_UNSUPPORTED, "f32 path"),
+])
+def test_attn_rejects(lib, kw, status, msg):
+    assert attn(lib, **kw) == status
+    assert msg in lib.rf_last_error().decode()
+
+
+def decode(lib, ws=P, ws_bytes=1 << 30, B=2, Hq=16, Hkv=2, L=100, D=128, S_=4, dt=2, q=P, o=P):
+    return lib.rf_attn_decode_splitkv(q, P, P, o, None, ws, ws_bytes, B, Hq, Hkv, L, D, S_, 0.1, dt, S)
+
+
+@pytest.mark.parametrize("kw,status,msg", [
+    (dict(ws=None), rf.RF_ERR_INVALID_ARG, "non-null"),
+    (dict(q=None), rf.RF_ERR_INVALID_ARG, "non-null"),
+    (dict(L=0), rf.RF_ERR_INVALID_ARG, "positive"),
+    (dict(S_=0), rf.RF_ERR_INVALID_ARG, "positive"),
+    (dict(Hq=15), rf.RF_ERR_INVALID_ARG, "multiple"),
+    (dict(ws=ctypes.c_void_p(0x10010)), rf.RF_ERR_INVALID_ARG, "256-byte"),
+    (dict(ws_bytes=100), rf.RF_ERR_INVALID_ARG, "too small"),
+    (dict(dt=0), rf.RF_ERR_UNSUPPORTED, "f32"),
+    (dict(D=96), rf.RF_ERR_UNSUPPORTED, "D must be"),
+    (dict(Hq=32, Hkv=2), rf.RF_ERR_UNSUPPORTED, "at most 8"),
+    (dict(S_=300), rf.RF_ERR_UNSUPPORTED, "256"),
+])
+def test_decode_rejects(lib, kw, status, msg):
+    assert decode(lib, **kw) == status
+    assert msg in lib.rf_last_error().decode()
+
+
+def test_decode_workspace_size(lib):
+    B, Hq, D, S_ = 16, 64, 128, 16
+    n = lib.rf_attn_decode_splitkv_workspace_bytes(B, Hq, D, S_)
+    o_bytes = B * Hq * S_ * D * 4
+    assert n == (o_bytes + 255) // 256 * 256 + B * Hq * S_ * 4
+    assert lib.rf_attn_decode_splitkv_workspace_bytes(0, Hq, D, S_) == 0
+    assert lib.rf_attn_decode_splitkv_workspace_bytes(B, Hq, D, -1) == 0
+
+
+@pytest.mark.parametrize("args,status,msg", [
+    ((None, P, P, None, 4, 2, 8, 1), rf.RF_ERR_INVALID_ARG, "non-null"),
+    ((P, P, P, None, 0, 2, 8, 1), rf.RF_ERR_INVALID_ARG, "positive"),
+    ((P, P, MIS, None, 4, 2, 8, 1), rf.RF_ERR_INVALID_ARG, "aligned"),
+    ((P, P, P, None, 4, 2, 6, 1), rf.RF_ERR_UNSUPPORTED, "multiple of 4"),
+    ((P, P, P, None, 4, 2, 516, 1), rf.RF_ERR_UNSUPPORTED, "multiple of 4"),
+    ((P, P, P, None, 4, 257, 8, 1), rf.RF_ERR_UNSUPPORTED, "256"),
+    ((P, P, P, None, 4, 2, 8, 9), rf.RF_ERR_INVALID_ARG, "dtype"),
+])
+def test_merge_rejects(lib, args, status, msg):
+    assert lib.rf_lse_merge(*args, S) == status
+    assert msg in lib.rf_last_error().decode()
+
+
+@pytest.mark.parametrize("args,status,msg", [
+    ((None, P, P, P, P, None, 4, 64, 1e-5, 2), rf.RF_ERR_INVALID_ARG, "non-null"),
+    ((P, P, P, P, None, None, 4, 64, 1e-5, 2), rf.RF_ERR_INVALID_ARG, "non-null"),
+    ((P, P, P, P, P, None, 0, 64, 1e-5, 2), rf.RF_ERR_INVALID_ARG, "positive"),
+    ((P, P, P, P, P, None, 4, 64, -1.0, 2), rf.RF_ERR_INVALID_ARG, "eps"),
+    ((P, P, P, P, P, MIS, 4, 64, 1e-5, 2), rf.RF_ERR_INVALID_ARG, "aligned"),
+    ((P, P, P, P, P, None, 4, 60, 1e-5, 2), rf.RF_ERR_INVALID_ARG, "multiple of 8"),
+    ((P, P, P, P, P, None, 4, 62, 1e-5, 0), rf.RF_ERR_INVALID_ARG, "multiple of 4"),
+    ((P, P, P, P, P, None, 4, 32776, 1e-5, 1), rf.RF_ERR_UNSUPPORTED, "exceeds 32768"),
+    ((P, P, P, P, P, None, 4, 16388, 1e-5, 0), rf.RF_ERR_UNSUPPORTED, "exceeds 16384"),
+])
+def test_layernorm_rejects(lib, args, status, msg):
+    assert lib.rf_layernorm_fused(*args, S) == status
+    assert msg in lib.rf_last_error().decode()
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+
+    x = torch.zeros(4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        rf.rf_layernorm_fused(x, x, None, None, x)
