@@ -34,7 +34,7 @@ def test_merge_shapes(rf, rows, S, D, dtype):
         check32(o, ro, "merge f32")
     else:
         check16(o, ro, "merge 16-bit")
-    check_lse(lse, rl, tol=1e-5 * max(1.0, float(np.abs(rl[np.isfinite(rl)]).max())))
+    check_lse(lse, rl, tol=1e-5 * max(1.0, float(np.abs(rl[np.isfinite(rl)]).max(initial=0.0))))
     empty = np.isneginf(rl)
     assert empty.any() and (o.float().numpy()[empty] == 0).all()
 
@@ -44,7 +44,11 @@ def test_merge_large_lse_values(rf):
     lse_part = lse_part * 50 + 300  # exp(lse) alone would overflow fp32
     o, lse = run(rf, o_part, lse_part, torch.float32)
     ro, rl = oracle.lse_merge(o_part, lse_part)
-    check32(o, ro, "large lse")
+    # fp32 floor: lse_s ~ 300 +- 200 is itself rounded to +-3e-5 absolute, so each
+    # weight exp(lse_s - LSE) carries ~3e-5 relative error: allow 1e-4 here.
+    rl2 = np.linalg.norm(o.numpy() - ro) / np.linalg.norm(ro)
+    mr = np.abs(o.numpy() - ro).max() / np.abs(ro).max()
+    assert rl2 <= 1e-5 and mr <= 1e-4, (rl2, mr)
     check_lse(lse, rl, tol=1e-5 * 1000)
 
 
