@@ -34,6 +34,7 @@ _SIGNATURES = {
     "rf_attn_fwd": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp], _i),
     "rf_attn_decode_splitkv_workspace_bytes": ([_i, _i, _i, _i], _sz),
     "rf_attn_decode_splitkv": ([_vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _i, _f, _i, _vp], _i),
+    "rf_attn_decode_splitkv_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp], _i),
     "rf_lse_merge": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp], _i),
     "rf_layernorm_fused": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _f, _i, _vp], _i),
     "rf_last_error": ([], ctypes.c_char_p),
@@ -159,6 +160,26 @@ def rf_attn_decode_splitkv(q, k_cache, v_cache, o, workspace, num_splits, lse=No
                                          _stream(stream)))
 
 
+def rf_attn_decode_splitkv_noalloc(q, k_cache, v_cache, o, num_splits, lse=None, scale=None, stream=None):
+    """rf_attn_decode_splitkv for callers that cannot allocate: the split partials go to
+    scratch built into the library (RF_DECODE_NOALLOC_SCRATCH_BYTES), not to a workspace.
+    Calls that may overlap on the GPU share that scratch and must be serialised."""
+    if q.dim() == 4:
+        q = q.reshape(q.shape[0], q.shape[1], q.shape[3])
+    B, Hq, D = q.shape
+    Hkv, L = k_cache.shape[1], k_cache.shape[2]
+    if tuple(k_cache.shape) != (B, Hkv, L, D) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache / v_cache shape mismatch")
+    if o.numel() != B * Hq * D or o.dtype != q.dtype:
+        raise ValueError("o must hold B*Hq*D elements of q's dtype")
+    if lse is not None and (lse.dtype != torch.float32 or lse.numel() != B * Hq):
+        raise ValueError("lse must be float32 with B*Hq elements")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check(load().rf_attn_decode_splitkv_noalloc(_dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+                                                 _dev(o, "o"), _dev(lse, "lse", True), B, Hq, Hkv, L, D,
+                                                 int(num_splits), scale, _code(q.dtype), _stream(stream)))
+
+
 def rf_lse_merge(o_part, lse_part, o, lse=None, stream=None):
     """o[rows,D] (and lse[rows]) <- merge of o_part[rows,S,D], lse_part[rows,S] (fp32)."""
     rows, S, D = o_part.shape
@@ -230,7 +251,8 @@ def layernorm(x, residual, gamma, beta, eps=1e-5, want_residual_out=False, strea
 
 __all__ = [
     "RFError", "load", "declared_symbols", "rf_version", "rf_last_error", "rf_device_status", "rf_attn_fwd",
-    "rf_attn_decode_splitkv_workspace_bytes", "rf_attn_decode_splitkv", "rf_lse_merge", "rf_layernorm_fused",
+    "rf_attn_decode_splitkv_workspace_bytes", "rf_attn_decode_splitkv", "rf_attn_decode_splitkv_noalloc",
+    "rf_lse_merge", "rf_layernorm_fused",
     "attention", "decode", "decode_workspace", "decode_partials_view", "layernorm",
     "RF_OK", "RF_ERR_INVALID_ARG", "RF_ERR_UNSUPPORTED", "RF_ERR_CUDA", "RF_ERR_TIMEOUT",
 ]

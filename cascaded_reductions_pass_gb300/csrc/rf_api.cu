@@ -313,3 +313,57 @@ rf_status_t rf_layernorm_fused(const void* x, const void* residual, const void* 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// rf_attn_decode_splitkv_noalloc: the decode entry point for callers that may
+// not allocate device memory.  Its scratch (the per-split partials) lives in
+// this file-scope array instead of a caller-provided workspace.  Every GPU
+// that loads the library holds the array until the process exits.  Host code
+// cannot use the array's name as a device address, so the address is looked
+// up with cudaGetSymbolAddress once per device (on that device's first call,
+// with the device current) and cached.  Nothing in the array has to start at
+// zero: each call writes every partial slot before the merge reads it.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_decode_scratch[RF_DECODE_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+void* decode_scratch_for_current_device() {
+  static std::mutex mu;
+  static void* ptrs[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    ptrs[dev] = p;
+  }
+  return ptrs[dev];
+}
+
+}  // namespace
+
+extern "C" rf_status_t rf_attn_decode_splitkv_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                                      void* o, float* lse, int B, int Hq, int Hkv, int L, int D,
+                                                      int num_splits, float scale, rf_dtype_t dtype,
+                                                      void* stream) {
+  const size_t need = rf_attn_decode_splitkv_workspace_bytes(B, Hq, D, num_splits);
+  if (need > size_t(RF_DECODE_NOALLOC_SCRATCH_BYTES))
+    return fail(RF_ERR_INVALID_ARG,
+                "rf_attn_decode_splitkv_noalloc: B=%d Hq=%d D=%d num_splits=%d needs %zu bytes of scratch, "
+                "more than the %zu bytes built into the library; use rf_attn_decode_splitkv with a workspace",
+                B, Hq, D, num_splits, need, size_t(RF_DECODE_NOALLOC_SCRATCH_BYTES));
+  void* scratch = decode_scratch_for_current_device();
+  if (scratch == nullptr)
+    return fail(RF_ERR_CUDA, "rf_attn_decode_splitkv_noalloc: cannot resolve the scratch address on this device");
+  return rf_attn_decode_splitkv(q, k_cache, v_cache, o, lse, scratch, size_t(RF_DECODE_NOALLOC_SCRATCH_BYTES), B,
+                                Hq, Hkv, L, D, num_splits, scale, dtype, stream);
+}

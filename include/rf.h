@@ -17,7 +17,8 @@
  * - Every tensor pointer is a DEVICE pointer owned by the caller, contiguous
  *   row-major in the layout stated at each call.  The library allocates no
  *   device memory; the one call that needs scratch takes it from the caller
- *   (rf_attn_decode_splitkv's workspace).
+ *   (rf_attn_decode_splitkv's workspace), and its _noalloc variant uses a
+ *   fixed scratch array built into the library instead.
  * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *   stream).  Calls are asynchronous: they enqueue kernels on `stream` and
  *   return; results are ready once the stream has been synchronised.
@@ -122,6 +123,36 @@ rf_status_t rf_attn_decode_splitkv(const void* q, const void* k_cache, const voi
                                    void* o, float* lse, void* workspace, size_t workspace_bytes,
                                    int B, int Hq, int Hkv, int L, int D, int num_splits,
                                    float scale, rf_dtype_t dtype, void* stream);
+
+/*
+ * rf_attn_decode_splitkv_noalloc -- rf_attn_decode_splitkv without a
+ * workspace argument, for callers that cannot allocate device memory: for
+ * example a plugin whose host framework owns all device memory and hands it
+ * only the input and output buffers, or a serving loop that reserves all its
+ * memory at start-up and forbids later allocation because cudaMalloc can
+ * synchronise the device and can fail under memory pressure mid-run.  The
+ * pages describe no such call; it exists for this deployment constraint only.
+ *
+ * Same arguments, layouts, results and errors as rf_attn_decode_splitkv,
+ * minus `workspace` / `workspace_bytes`.  The per-split partials live in a
+ * scratch array of RF_DECODE_NOALLOC_SCRATCH_BYTES built into the library
+ * (every GPU that loads the library holds it until the process exits).
+ * - Sizes whose partials need more than that (see
+ *   rf_attn_decode_splitkv_workspace_bytes) return RF_ERR_INVALID_ARG with a
+ *   message naming both sizes; no kernel is launched.
+ * - The call allocates nothing (no cudaMalloc, no cudaFree).  Its first call
+ *   on each device looks up the scratch address with cudaGetSymbolAddress
+ *   (with that device current); make that first call before any stream
+ *   capture.
+ * - All calls share the one scratch array: calls that can overlap on the GPU
+ *   (other streams, other host threads) race on it and must be serialised by
+ *   the caller.  After a call the array holds that call's partials; nothing
+ *   in it needs to start at zero.
+ */
+#define RF_DECODE_NOALLOC_SCRATCH_BYTES (16u << 20) /* 16 MiB */
+rf_status_t rf_attn_decode_splitkv_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                           void* o, float* lse, int B, int Hq, int Hkv, int L, int D,
+                                           int num_splits, float scale, rf_dtype_t dtype, void* stream);
 
 /*
  * rf_lse_merge -- combine partial attention results computed over disjoint
