@@ -122,11 +122,16 @@ class ClockSampler:
 class Runner:
     """One workload: its inputs on the device, one step of the hot path, its work."""
 
-    def __init__(self, name, dev):
+    def __init__(self, name, dev, batch=None):
+        import dataclasses
+
         import cascaded_reductions_pass_gb300 as rf
 
         self.rf = rf
         self.w = inputs.WORKLOADS[name]
+        if batch:  # a smaller case of the same kernel (for profiler captures)
+            key = "rows" if self.w.kind == "layernorm" else "B"
+            self.w = dataclasses.replace(self.w, dims={**self.w.dims, key: int(batch)})
         self.dev = dev
         d = self.w.dims
         self.host = inputs.make(self.w)
@@ -300,8 +305,8 @@ def cpu_threads():
 
 
 # ----------------------------------------------------------------------------- main
-def measure(name, dev, steps, warmup, flush, peaks, with_e2e=True):
-    r = Runner(name, dev)
+def measure(name, dev, steps, warmup, flush, peaks, with_e2e=True, batch=None):
+    r = Runner(name, dev, batch)
     times = time_steps(r, steps, warmup, flush)
     ms = float(np.mean(times))
     val = r.units / (ms / 1e3)
@@ -328,6 +333,20 @@ def measure(name, dev, steps, warmup, flush, peaks, with_e2e=True):
     return r, res
 
 
+def aggregate_over_ranks(local_ms, units_per_rank, world, device=None):
+    """Replicas: every rank processed `units_per_rank`; the job's time is the slowest
+    rank's.  Returns (max_ms, whole-job value in units/s).  With world > 1 this is a
+    MAX all-reduce of one scalar -- the only collective, and it is outside the data path."""
+    ms = float(local_ms)
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * units_per_rank / (ms / 1e3)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -337,6 +356,9 @@ def main():
     ap.add_argument("--workload", default="attn_fwd_f16_d64", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--no-parts", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override B (attention, decode) or rows (LayerNorm): a smaller case for profiler captures")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -386,24 +408,19 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
-    runner, res = measure(args.workload, dev, args.steps, args.warmup, flush, peaks, with_e2e=False)
+    runner, res = measure(args.workload, dev, args.steps, args.warmup, flush, peaks, with_e2e=False,
+                          batch=args.batch)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     t1 = time.time()
-    total_ms = sum([res["ms_per_step"]]) * args.steps
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
-    ms = total_ms / args.steps
-    value = world * runner.units / (ms / 1e3)
-    e_ms, h2d, d2h = time_e2e(runner, max(3, min(args.steps, 10)), 3)
-    e2e_val = runner.units / (e_ms / 1e3)
-    if world > 1:
-        et = torch.tensor([e_ms], device=dev)
-        dist.all_reduce(et, op=dist.ReduceOp.MAX)
-        e2e_val = world * runner.units / (float(et.item()) / 1e3)
+    ms, value = aggregate_over_ranks(res["ms_per_step"], runner.units, world, dev)
+    e2e = None
+    if not args.no_e2e:
+        e_ms, h2d, d2h = time_e2e(runner, max(3, min(args.steps, 10)), 3)
+        e_ms, e2e_val = aggregate_over_ranks(e_ms, runner.units, world, dev)
+        e2e = {"value": e2e_val, "unit": runner.unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e_ms}
     clocks = sampler.summary(t0, t1)
     launches = args.steps * (2 if w.kind == "decode" else 1)
 
@@ -435,8 +452,7 @@ def main():
             "config": {**runner.describe(), "l2": "flushed before every step (512 MiB memset, outside the events)",
                        "parallelism": f"replicas{world}" if world > 1 else "single-gpu"},
             "roofline": res["roofline"],
-            "e2e": {"value": e2e_val, "unit": runner.unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e_ms},
+            "e2e": e2e,
             "gpu_launches": launches, "clocks": clocks, "cpu_baseline": cpu,
             "device_status": int(status), "parts": parts,
             "ms_p10": res["ms_p10"], "ms_p90": res["ms_p90"],

@@ -1,8 +1,381 @@
-// attn_fwd_tc.cu -- placeholder until the tcgen05 attention kernel lands.
+// attn_fwd_tc.cu -- attention forward on the 5th-generation tensor cores
+// (tcgen05 + TMEM + TMA) for fp16/bf16 inputs, D in {64, 128}.
+//
+// The cascade max -> sum exp -> sum exp*v (RedFuser, Abstract: safe softmax
+// followed by GEMM; "Operator Fusion" guide, section 2, Pattern 4) runs as one
+// loop over 128-key tiles in the incremental form of RedFuser's Figure 4:
+// level 1 (reduce max, combine +) keeps a running row max m; levels 2 and 3
+// (reduce +, combine *) keep the running sum l and the running output O, both
+// corrected by exp(m_old - m_new) when m rises.  The correction is applied
+// lazily: m moves only when a tile's max exceeds it by more than 2^8 (in
+// base 2), which stays exact because l and O are built against the same m, and
+// keeps P <= 256.
+//
+// CTA = two query tiles of 128 rows (rows r0..r0+255 of one (batch, head)),
+// 12 warps:
+//   warp 0      TMA producer: Q once; K and V tiles through 2-3 stage rings.
+//   warp 1      allocates 512 TMEM columns; lane 0 issues every tcgen05.mma.
+//   warps 4-7   softmax for query tile 0, warps 8-11 for tile 1: one thread
+//               per query row, i.e. per TMEM lane, so row max and row sum need
+//               no cross-thread reduction.
+// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D).
+// P (16-bit, two per column) overwrites the first 64 columns of its S tile and
+// feeds O += P V as the TMEM A operand.  The MMA order per key tile j is
+// PV0_j, S0_{j+1}, PV1_j, S1_{j+1}: the tensor core works on one tile while
+// the other tile's softmax runs (ping-pong).  A tcgen05.commit after S_t(j+1)
+// also covers PV_t(j), so when softmax t sees S, O_t is final up to tile j and
+// may be rescaled in place before PV_t(j+1) is issued.
+//
+// Shared memory operands use the 128-byte swizzle written by TMA: Q and K
+// K-major (boxes of 64 dims x 128 rows), V MN-major (the same boxes read as
+// D x keys).  Causal CTAs are scheduled longest-first, and the query heads of
+// one GQA group are adjacent in launch order so their K/V tiles hit in L2.
+// Every mbarrier wait is bounded; on a timeout the CTA records RF_ERR_TIMEOUT,
+// waits (bounded) for its copies and MMAs in flight, frees TMEM and exits.
+#include <cuda.h>
+#include <math.h>
+
 #include "rf_device.cuh"
+
 namespace rf {
-cudaError_t launch_attn_tc(const void*, const void*, const void*, void*, float*, int, int, int, int, int, int,
-                           float, int, Dt, unsigned*, cudaStream_t) {
+namespace {
+
+constexpr int kBM = 128;        // query rows per tile (TMEM lanes)
+constexpr int kBN = 128;        // keys per tile
+constexpr int kThreads = 384;   // 12 warps
+constexpr int kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // base-2 units
+
+template <int D>
+struct Cfg {
+  static constexpr int kQBytes = kBM * D * 2;    // one query tile
+  static constexpr int kKVBytes = kBN * D * 2;   // one K or V tile
+  static constexpr int kStages = D == 64 ? 3 : 2;
+  static constexpr int kTiles = 2 * kQBytes + 2 * kStages * kKVBytes;
+};
+
+struct alignas(8) TcBars {
+  uint64_t q_full;
+  uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];
+  uint64_t s_full[2], p_ready[2], o_final[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, unsigned parity) {
+  const bool ok = mbar_wait(bar, parity);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <Dt DT, int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                   const __grid_constant__ CUtensorMap tv, uint16_t* __restrict__ o, float* __restrict__ lse,
+                   int Hq, int Hkv, int Nq, int Nk, int BH, int nqt, float sl2, unsigned* status) {
+  using C = Cfg<D>;
+  constexpr int S = C::kStages;
+  constexpr bool kBF16 = DT == Dt::BF16;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK = sQ + 2 * C::kQBytes;
+  uint8_t* sV = sK + S * C::kKVBytes;
+  TcBars* bars = reinterpret_cast<TcBars*>(sV + S * C::kKVBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int id = blockIdx.x;
+  const int c = nqt - 1 - id / BH;  // longest-first for causal
+  const int bh = id - (id / BH) * BH;
+  const int h = bh % Hq, b = bh / Hq;
+  const int kv_plane = b * Hkv + h / (Hq / Hkv);
+  const int r0 = c * 2 * kBM;
+  const int n_kv = (Nk + kBN - 1) / kBN;
+  const int nt0 = CAUSAL ? min(r0 / kBN + 1, n_kv) : n_kv;
+  const int nt1 = CAUSAL ? min(r0 / kBN + 2, n_kv) : n_kv;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->v_empty[i], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_ready[t], 4 * 32);
+      mbar_init(&bars->o_final[t], 1);
+    }
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc_alloc(&bars->tmem_base, kTmemCols);
+    tc_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      mbar_expect_tx(&bars->q_full, 2 * C::kQBytes);
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int bx = 0; bx < D / 64; ++bx)
+          tma_load_3d(sQ + t * C::kQBytes + bx * (kBM * 128), &tq, &bars->q_full, bx * 64, r0 + t * kBM, bh);
+      int issued_k = 0, issued_v = 0;
+      bool ok = true;
+      for (int j = 0; j < nt1; ++j) {
+        const int st = j % S;
+        if (j >= S && !(ok = mbar_wait(&bars->k_empty[st], ((j / S) - 1) & 1))) break;
+        mbar_expect_tx(&bars->k_full[st], C::kKVBytes);
+#pragma unroll
+        for (int bx = 0; bx < D / 64; ++bx)
+          tma_load_3d(sK + st * C::kKVBytes + bx * (kBN * 128), &tk, &bars->k_full[st], bx * 64, j * kBN, kv_plane);
+        ++issued_k;
+        if (j >= S && !(ok = mbar_wait(&bars->v_empty[st], ((j / S) - 1) & 1))) break;
+        mbar_expect_tx(&bars->v_full[st], C::kKVBytes);
+#pragma unroll
+        for (int bx = 0; bx < D / 64; ++bx)
+          tma_load_3d(sV + st * C::kKVBytes + bx * (kBN * 128), &tv, &bars->v_full[st], bx * 64, j * kBN, kv_plane);
+        ++issued_v;
+      }
+      if (!ok) {
+        atomicOr(status, kStatusTimeout);
+        bars->abort = 1;
+      }
+      // every copy issued must land before the CTA exits
+      bool drained = mbar_wait(&bars->q_full, 0);
+      for (int j = issued_k > S ? issued_k - S : 0; j < issued_k; ++j)
+        drained &= mbar_wait(&bars->k_full[j % S], (j / S) & 1);
+      for (int j = issued_v > S ? issued_v - S : 0; j < issued_v; ++j)
+        drained &= mbar_wait(&bars->v_full[j % S], (j / S) & 1);
+      if (!drained) atomicOr(status, kStatusTimeout);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK), va = smem_u32(sV);
+      constexpr uint32_t idS = tc_idesc_f16(kBF16, kBM, kBN, false);
+      constexpr uint32_t idPV = tc_idesc_f16(kBF16, kBM, D, true);
+      auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T  (M=128, N=128, K=D)
+        const uint32_t qbase = qa + t * C::kQBytes, kbase = ka + (j % S) * C::kKVBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off_q = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+          const uint32_t off_k = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
+          tc_mma_ss(tmem + t * kBN, tc_sdesc_sw128(qbase + off_q, 16, 1024), tc_sdesc_sw128(kbase + off_k, 16, 1024),
+                    idS, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int t, int j) {  // O_t += P_t V_j  (M=128, N=D, K=128; P from TMEM)
+        const uint32_t vbase = va + (j % S) * C::kKVBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          tc_mma_ts(tmem + 2 * kBN + t * D, tmem + t * kBN + kk * 8,
+                    tc_sdesc_sw128(vbase + kk * 16 * 128, kBN * 128, 1024), idPV, (j > 0 || kk > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(&bars->q_full, 0) && mbar_wait(&bars->k_full[0], 0);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        tc_commit(&bars->s_full[0]);
+        issue_s(1, 0);
+        tc_commit(&bars->s_full[1]);
+        tc_commit(&bars->k_empty[0]);
+      }
+      for (int j = 0; ok && j < nt1; ++j) {
+        const int st = j % S, jn = j + 1, stn = jn % S;
+        if (!(ok = mbar_wait(&bars->v_full[st], (j / S) & 1))) break;
+        if (j < nt0) {
+          if (!(ok = mbar_wait(&bars->p_ready[0], j & 1))) break;
+          tc_fence_after();
+          issue_pv(0, j);
+          if (j == nt0 - 1) tc_commit(&bars->o_final[0]);
+        }
+        bool k_ready = false;
+        if (jn < nt0) {
+          if (!(ok = mbar_wait(&bars->k_full[stn], (jn / S) & 1))) break;
+          k_ready = true;
+          tc_fence_after();
+          issue_s(0, jn);
+          tc_commit(&bars->s_full[0]);
+        }
+        if (!(ok = mbar_wait(&bars->p_ready[1], j & 1))) break;
+        tc_fence_after();
+        issue_pv(1, j);
+        if (j == nt1 - 1) tc_commit(&bars->o_final[1]);
+        tc_commit(&bars->v_empty[st]);
+        if (jn < nt1) {
+          if (!k_ready) {
+            if (!(ok = mbar_wait(&bars->k_full[stn], (jn / S) & 1))) break;
+            tc_fence_after();
+          }
+          issue_s(1, jn);
+          tc_commit(&bars->s_full[1]);
+          tc_commit(&bars->k_empty[stn]);
+        }
+      }
+      if (!ok) {
+        atomicOr(status, kStatusTimeout);
+        bars->abort = 1;
+      }
+      // every MMA issued must complete before TMEM is released
+      tc_commit(&bars->drain);
+      if (!mbar_wait(&bars->drain, 0)) atomicOr(status, kStatusTimeout);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax (one thread per query row)
+    const int t = (warp - 4) >> 2;
+    const int qw = warp & 3;
+    const int row = r0 + t * kBM + qw * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
+    const uint32_t tS = tmem + lane_off + t * kBN;
+    const uint32_t tO = tmem + lane_off + 2 * kBN + t * D;
+    const int n = t == 0 ? nt0 : nt1;
+    const int tile_row0 = r0 + t * kBM;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      if (!(ok = warp_wait(&bars->s_full[t], j & 1))) break;
+      tc_fence_after();
+      uint32_t s[kBN];
+#pragma unroll
+      for (int i = 0; i < kBN / 32; ++i) tc_ld32(tS + 32 * i, s + 32 * i);
+      tc_wait_ld();
+      const int key0 = j * kBN;
+      if (key0 + kBN > Nk || (CAUSAL && key0 + kBN - 1 > tile_row0)) {
+        const int lim = CAUSAL ? min(Nk, row + 1) : Nk;  // keys [key0, lim) are visible
+#pragma unroll
+        for (int i = 0; i < kBN; ++i)
+          if (key0 + i >= lim) s[i] = __float_as_uint(-INFINITY);
+      }
+      // level 1: tile max (one thread owns the whole row)
+      float mx = __uint_as_float(s[0]);
+#pragma unroll
+      for (int i = 1; i < kBN; ++i) mx = fmaxf(mx, __uint_as_float(s[i]));
+      const float mt = mx * sl2;
+      const bool need = mt > m_run + kRescaleThreshold;
+      const float m_new = need ? mt : m_run;
+      const float alpha = exp2f(m_run - m_new);
+      // level 2: P = exp(s - m) to TMEM (16-bit, over the S columns), running sum
+      float sum = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < kBN / 16; ++cc) {
+        uint32_t pk[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float p0 = exp2f(fmaf(__uint_as_float(s[16 * cc + 2 * e]), sl2, -m_new));
+          const float p1 = exp2f(fmaf(__uint_as_float(s[16 * cc + 2 * e + 1]), sl2, -m_new));
+          sum += p0 + p1;
+          pk[e] = Pack<DT>::pack2(p0, p1);
+        }
+        tc_st8(tS + 8 * cc, pk);
+      }
+      l_run = fmaf(l_run, alpha, sum);
+      // level 3 correction: rescale O in TMEM when some row's max moved
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) {
+          uint32_t ov[32];
+          tc_ld32(tO + 32 * i, ov);
+          tc_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+          tc_st32(tO + 32 * i, ov);
+        }
+      }
+      m_run = m_new;
+      tc_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->p_ready[t]);
+    }
+    if (ok) ok = warp_wait(&bars->o_final[t], 0);
+    if (ok) {
+      // epilogue: O / l in the output dtype, LSE in natural log
+      tc_fence_after();
+      const float inv = 1.0f / l_run;
+      const bool row_ok = row < Nq;
+      uint4* orow = reinterpret_cast<uint4*>(o + (static_cast<long long>(bh) * Nq + (row_ok ? row : 0)) * D);
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) {
+        uint32_t ov[32];
+        tc_ld32(tO + 32 * i, ov);
+        tc_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = Pack<DT>::pack2(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
+        if (row_ok) {
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            orow[i * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        }
+      }
+      if (row_ok && lse) lse[static_cast<long long>(bh) * Nq + row] = (m_run + log2f(l_run)) * kLn2;
+    } else {
+      if (lane == 0) atomicOr(status, kStatusTimeout);
+      bars->abort = 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tc_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <Dt DT, int D, bool CAUSAL>
+cudaError_t launch_cfg(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                       int Nq, int Nk, float scale, unsigned* status, cudaStream_t s) {
+  alignas(64) CUtensorMap tq, tk, tv;
+  cudaError_t err = cudaSuccess;
+  if (!encode_tma_3d_16bit(&tq, q, D, Nq, uint64_t(B) * Hq, kBM, &err)) return err;
+  if (!encode_tma_3d_16bit(&tk, k, D, Nk, uint64_t(B) * Hkv, kBN, &err)) return err;
+  if (!encode_tma_3d_16bit(&tv, v, D, Nk, uint64_t(B) * Hkv, kBN, &err)) return err;
+  const int nqt = (Nq + 2 * kBM - 1) / (2 * kBM);
+  const long long grid = static_cast<long long>(nqt) * B * Hq;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const int smem = Cfg<D>::kTiles + 1024 + static_cast<int>(sizeof(TcBars)) + 64;
+  auto kern = attn_tc_kernel<DT, D, CAUSAL>;
+  err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  kern<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(tq, tk, tv, static_cast<uint16_t*>(o), lse, Hq, Hkv, Nq,
+                                                           Nk, B * Hq, nqt, scale * kLog2e, status);
+  return cudaGetLastError();
+}
+
+template <Dt DT, int D>
+cudaError_t launch_d(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                     int Nq, int Nk, float scale, int causal, unsigned* status, cudaStream_t s) {
+  return causal ? launch_cfg<DT, D, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, status, s)
+                : launch_cfg<DT, D, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, status, s);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                           int Nq, int Nk, int D, float scale, int causal, Dt dt, unsigned* status, cudaStream_t s) {
+  if (dt == Dt::BF16)
+    return D == 128 ? launch_d<Dt::BF16, 128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, status, s)
+                    : launch_d<Dt::BF16, 64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, status, s);
+  if (dt == Dt::F16)
+    return D == 128 ? launch_d<Dt::F16, 128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, status, s)
+                    : launch_d<Dt::F16, 64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, status, s);
   return cudaErrorNotSupported;
 }
+
 }  // namespace rf

@@ -1,0 +1,104 @@
+"""GPU parity of rf_attn_fwd's tcgen05 path (fp16/bf16, D in {64, 128}) against the
+fp64 oracle, through the C ABI.  Small and ragged shapes are compared element by
+element; the two full-size workloads on sampled query rows."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from cascaded_reductions_pass_gb300 import inputs
+from _parity import check16, check_lse, to64
+from test_golden import dec
+
+pytestmark = pytest.mark.gpu
+
+
+def run(rf, q, k, v, scale, causal):
+    o, lse = rf.attention(q.cuda(), k.cuda(), v.cuda(), scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    return o.cpu(), lse.cpu()
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,D,causal,dtype", [
+    (1, 1, 1, 128, 128, 64, False, "f16"),
+    (1, 1, 1, 128, 128, 128, False, "bf16"),
+    (1, 2, 1, 256, 256, 64, True, "f16"),
+    (1, 2, 2, 200, 200, 128, False, "bf16"),   # ragged tiles
+    (2, 4, 2, 384, 384, 128, True, "bf16"),    # GQA, causal, 1.5 CTA tiles
+    (1, 1, 1, 1, 1, 64, False, "f16"),
+    (1, 1, 1, 1, 1, 128, True, "bf16"),
+    (1, 3, 1, 1000, 1000, 64, True, "bf16"),
+    (1, 2, 1, 64, 64, 128, True, "f16"),
+    (1, 2, 2, 100, 700, 64, False, "f16"),     # Nq != Nk
+    (1, 2, 1, 513, 300, 128, False, "f16"),
+    (1, 4, 4, 1024, 1024, 64, False, "bf16"),
+    (1, 8, 2, 640, 640, 128, True, "f16"),
+])
+def test_shapes(rf, B, Hq, Hkv, Nq, Nk, D, causal, dtype):
+    q, k, v = inputs.attn_inputs(B, Hq, Hkv, Nq, Nk, D, dtype, seed=Nq + Nk + D)
+    scale = float(np.float32(1 / np.sqrt(D)))
+    o, lse = run(rf, q, k, v, scale, causal)
+    ro, rl = oracle.attention(q, k, v, scale, causal)
+    check16(o, ro, f"{dtype} D={D} causal={causal}")
+    check_lse(lse, rl, what="lse")
+
+
+def test_golden_fixture(rf):
+    with open(os.path.join(os.path.dirname(__file__), "golden", "attn_small_oracle.json")) as f:
+        g = json.load(f)
+    q, k, v = (torch.from_numpy(dec(g[n]).astype(np.float32)).to(torch.float16) for n in ("q", "k", "v"))
+    for causal in (0, 1):
+        o, lse = run(rf, q, k, v, g["scale"], bool(causal))
+        check16(o, dec(g[f"o_causal{causal}"]), f"golden causal={causal}")
+        check_lse(lse, dec(g[f"lse_causal{causal}"]), what="golden lse")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_softmax_rows_sum_to_one(rf, causal):
+    # V = identity (Nk = D = 64): each output row is the softmax row itself.
+    q, k, _ = inputs.attn_inputs(1, 2, 2, 64, 64, 64, "bf16", seed=40)
+    v = torch.eye(64, dtype=torch.bfloat16).expand(1, 2, 64, 64).contiguous()
+    o, _ = run(rf, q * 3, k, v, 0.125, causal)
+    s = to64(o).sum(-1)
+    assert np.abs(s - 1).max() <= 2e-2
+    if causal:
+        assert (np.triu(to64(o)[0, 0], 1) == 0).all()
+
+
+def test_constant_v_and_large_scores(rf):
+    q, k, _ = inputs.attn_inputs(1, 2, 1, 500, 500, 128, "f16", seed=41)
+    row = torch.randn(128).to(torch.float16)
+    v = row.expand(1, 1, 500, 128).contiguous()
+    o, _ = run(rf, q * 4, k * 4, v, 1.0, True)  # scores of several hundred: exp must not overflow
+    assert np.abs(to64(o) - to64(row)).max() <= 2e-2
+
+
+def test_one_hot_dominant_key(rf):
+    q, k, v = inputs.attn_inputs(1, 1, 1, 256, 256, 64, "bf16", seed=42)
+    targets = torch.randperm(256, generator=torch.Generator().manual_seed(0))
+    q2 = (k[0, 0, targets].float() * 8).to(torch.bfloat16)[None, None]
+    o, _ = run(rf, q2, k, v, 1.0, False)
+    check16(o[0, 0], to64(v[0, 0, targets]), "one-hot")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["attn_fwd_f16_d64", "attn_fwd_causal_gqa_bf16_d128"])
+def test_full_size_sampled(rf, name):
+    w = inputs.WORKLOADS[name]
+    d = w.dims
+    q, k, v = inputs.make(w)
+    scale = float(np.float32(1 / np.sqrt(d["D"])))
+    o, lse = run(rf, q, k, v, scale, bool(d["causal"]))
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 255, 256, d["N"] - 1], rng.integers(0, d["N"], 57)]))
+    G = d["Hq"] // d["Hkv"]
+    for b, h in [(0, 0), (d["B"] - 1, d["Hq"] - 1), (0, d["Hq"] // 2 + 1)]:
+        kv = h // G
+        ro, rl = oracle.attention(q[b:b + 1, h:h + 1], k[b:b + 1, kv:kv + 1], v[b:b + 1, kv:kv + 1], scale,
+                                  bool(d["causal"]), rows=rows)
+        check16(o[b:b + 1, h:h + 1, rows], ro, f"{name} b={b} h={h}")
+        check_lse(lse[b:b + 1, h:h + 1, rows], rl, what=f"{name} lse")
