@@ -18,13 +18,20 @@
 //   warps 4-7   softmax for query tile 0, warps 8-11 for tile 1: one thread
 //               per query row, i.e. per TMEM lane, so row max and row sum need
 //               no cross-thread reduction.
-// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D).
-// P (16-bit, two per column) overwrites the first 64 columns of its S tile and
-// feeds O += P V as the TMEM A operand.  The MMA order per key tile j is
-// PV0_j, S0_{j+1}, PV1_j, S1_{j+1}: the tensor core works on one tile while
-// the other tile's softmax runs (ping-pong).  A tcgen05.commit after S_t(j+1)
-// also covers PV_t(j), so when softmax t sees S, O_t is final up to tile j and
-// may be rescaled in place before PV_t(j+1) is issued.
+// Registers are re-split after launch: warps 0-3 drop to 64 per thread and
+// the softmax warps rise to 216 (a row of S is 128 registers).
+//
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D).
+//  * D = 64: P0 [384,448) and P1 [448,512) have columns of their own (16-bit,
+//    two per column).  Softmax frees S_t as soon as it has loaded it, so the
+//    MMA issuer runs S_t(j+1) while softmax still exponentiates tile j; PV_t(j)
+//    follows once P_t(j) is ready.  Softmax waits for PV_t(j-1) to complete
+//    before it overwrites P_t or rescales O_t.
+//  * D = 128: no spare columns; P_t overwrites the first 64 columns of S_t and
+//    the order per key tile is PV0_j, S0_{j+1}, PV1_j, S1_{j+1}, so the tensor
+//    core works on one tile while the other tile's softmax runs (ping-pong).
+//    A commit after S_t(j+1) then also covers PV_t(j).
+// In both cases P is the TMEM A operand of O += P V.
 //
 // Shared memory operands use the 128-byte swizzle written by TMA: Q and K
 // K-major (boxes of 64 dims x 128 rows), V MN-major (the same boxes read as
@@ -47,6 +54,8 @@ constexpr int kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // base-2 units
+constexpr int kRegsCtl = 64;       // per thread, warps 0-3 after reallocation
+constexpr int kRegsSoftmax = 216;  // per thread, warps 4-11 after reallocation
 
 template <int D>
 struct Cfg {
@@ -54,12 +63,15 @@ struct Cfg {
   static constexpr int kKVBytes = kBN * D * 2;   // one K or V tile
   static constexpr int kStages = D == 64 ? 3 : 2;
   static constexpr int kTiles = 2 * kQBytes + 2 * kStages * kKVBytes;
+  static constexpr bool kSepP = D == 64;         // P in columns of its own
+  static constexpr int kOCol = 2 * kBN;          // O0 at 256, O1 at 256 + D
+  static constexpr int kPCol = 2 * kBN + 2 * D;  // P0 at 384, P1 at 448 (D = 64)
 };
 
 struct alignas(8) TcBars {
   uint64_t q_full;
   uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];
-  uint64_t s_full[2], p_ready[2], o_final[2];
+  uint64_t s_full[2], s_free[2], p_ready[2], pv_done[2], o_final[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -106,7 +118,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->s_free[t], 4 * 32);
       mbar_init(&bars->p_ready[t], 4 * 32);
+      mbar_init(&bars->pv_done[t], 1);
       mbar_init(&bars->o_final[t], 1);
     }
     mbar_init(&bars->drain, 1);
@@ -122,9 +136,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+  // Register split: 128 x 64 (producer / MMA warpgroup) + 256 x 216 (softmax)
+  // = 63,488 <= 384 x 168 registers granted at launch.
+  static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= kThreads * 168, "register split exceeds the launch budget");
+  if (warp < 4) {
+    regs_dec<kRegsCtl>();
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------- TMA producer
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
@@ -162,10 +180,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = issued_v > S ? issued_v - S : 0; j < issued_v; ++j)
         drained &= mbar_wait(&bars->v_full[j % S], (j / S) & 1);
       if (!drained) atomicOr(status, kStatusTimeout);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
       const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK), va = smem_u32(sV);
       constexpr uint32_t idS = tc_idesc_f16(kBF16, kBM, kBN, false);
       constexpr uint32_t idPV = tc_idesc_f16(kBF16, kBM, D, true);
@@ -181,9 +197,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto issue_pv = [&](int t, int j) {  // O_t += P_t V_j  (M=128, N=D, K=128; P from TMEM)
         const uint32_t vbase = va + (j % S) * C::kKVBytes;
+        const uint32_t pcol = C::kSepP ? C::kPCol + t * (kBN / 2) : t * kBN;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          tc_mma_ts(tmem + 2 * kBN + t * D, tmem + t * kBN + kk * 8,
+          tc_mma_ts(tmem + C::kOCol + t * D, tmem + pcol + kk * 8,
                     tc_sdesc_sw128(vbase + kk * 16 * 128, kBN * 128, 1024), idPV, (j > 0 || kk > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(&bars->q_full, 0) && mbar_wait(&bars->k_full[0], 0);
@@ -197,34 +214,68 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int j = 0; ok && j < nt1; ++j) {
         const int st = j % S, jn = j + 1, stn = jn % S;
-        if (!(ok = mbar_wait(&bars->v_full[st], (j / S) & 1))) break;
-        if (j < nt0) {
-          if (!(ok = mbar_wait(&bars->p_ready[0], j & 1))) break;
-          tc_fence_after();
-          issue_pv(0, j);
-          if (j == nt0 - 1) tc_commit(&bars->o_final[0]);
-        }
         bool k_ready = false;
-        if (jn < nt0) {
-          if (!(ok = mbar_wait(&bars->k_full[stn], (jn / S) & 1))) break;
-          k_ready = true;
-          tc_fence_after();
-          issue_s(0, jn);
-          tc_commit(&bars->s_full[0]);
-        }
-        if (!(ok = mbar_wait(&bars->p_ready[1], j & 1))) break;
-        tc_fence_after();
-        issue_pv(1, j);
-        if (j == nt1 - 1) tc_commit(&bars->o_final[1]);
-        tc_commit(&bars->v_empty[st]);
-        if (jn < nt1) {
-          if (!k_ready) {
-            if (!(ok = mbar_wait(&bars->k_full[stn], (jn / S) & 1))) break;
+        if constexpr (C::kSepP) {
+          // S_t(j+1) as soon as softmax t has read S_t(j); PV_t(j) once P_t(j) is ready.
+          if (jn < nt0) {
+            if (!(ok = mbar_wait(&bars->s_free[0], j & 1) && mbar_wait(&bars->k_full[stn], (jn / S) & 1))) break;
+            k_ready = true;
             tc_fence_after();
+            issue_s(0, jn);
+            tc_commit(&bars->s_full[0]);
           }
-          issue_s(1, jn);
-          tc_commit(&bars->s_full[1]);
-          tc_commit(&bars->k_empty[stn]);
+          if (!(ok = mbar_wait(&bars->v_full[st], (j / S) & 1))) break;
+          if (j < nt0) {
+            if (!(ok = mbar_wait(&bars->p_ready[0], j & 1))) break;
+            tc_fence_after();
+            issue_pv(0, j);
+            tc_commit(&bars->pv_done[0]);
+            if (j == nt0 - 1) tc_commit(&bars->o_final[0]);
+          }
+          if (jn < nt1) {
+            if (!(ok = mbar_wait(&bars->s_free[1], j & 1))) break;
+            if (!k_ready && !(ok = mbar_wait(&bars->k_full[stn], (jn / S) & 1))) break;
+            tc_fence_after();
+            issue_s(1, jn);
+            tc_commit(&bars->s_full[1]);
+            tc_commit(&bars->k_empty[stn]);
+          }
+          if (!(ok = mbar_wait(&bars->p_ready[1], j & 1))) break;
+          tc_fence_after();
+          issue_pv(1, j);
+          tc_commit(&bars->pv_done[1]);
+          tc_commit(&bars->v_empty[st]);
+          if (j == nt1 - 1) tc_commit(&bars->o_final[1]);
+        } else {
+          // P aliases S: PV_t(j) must be issued before S_t(j+1) overwrites it.
+          if (!(ok = mbar_wait(&bars->v_full[st], (j / S) & 1))) break;
+          if (j < nt0) {
+            if (!(ok = mbar_wait(&bars->p_ready[0], j & 1))) break;
+            tc_fence_after();
+            issue_pv(0, j);
+            if (j == nt0 - 1) tc_commit(&bars->o_final[0]);
+          }
+          if (jn < nt0) {
+            if (!(ok = mbar_wait(&bars->k_full[stn], (jn / S) & 1))) break;
+            k_ready = true;
+            tc_fence_after();
+            issue_s(0, jn);
+            tc_commit(&bars->s_full[0]);
+          }
+          if (!(ok = mbar_wait(&bars->p_ready[1], j & 1))) break;
+          tc_fence_after();
+          issue_pv(1, j);
+          if (j == nt1 - 1) tc_commit(&bars->o_final[1]);
+          tc_commit(&bars->v_empty[st]);
+          if (jn < nt1) {
+            if (!k_ready) {
+              if (!(ok = mbar_wait(&bars->k_full[stn], (jn / S) & 1))) break;
+              tc_fence_after();
+            }
+            issue_s(1, jn);
+            tc_commit(&bars->s_full[1]);
+            tc_commit(&bars->k_empty[stn]);
+          }
         }
       }
       if (!ok) {
@@ -235,16 +286,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit(&bars->drain);
       if (!mbar_wait(&bars->drain, 0)) atomicOr(status, kStatusTimeout);
     }
-  } else if (warp >= 4) {
+  } else {
+    regs_inc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax (one thread per query row)
     const int t = (warp - 4) >> 2;
     const int qw = warp & 3;
     const int row = r0 + t * kBM + qw * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
     const uint32_t tS = tmem + lane_off + t * kBN;
-    const uint32_t tO = tmem + lane_off + 2 * kBN + t * D;
+    const uint32_t tP = tmem + lane_off + (C::kSepP ? C::kPCol + t * (kBN / 2) : t * kBN);
+    const uint32_t tO = tmem + lane_off + C::kOCol + t * D;
     const int n = t == 0 ? nt0 : nt1;
     const int tile_row0 = r0 + t * kBM;
+    const uint64_t sl2x2 = f2pack(sl2, sl2);
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
@@ -254,6 +308,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < kBN / 32; ++i) tc_ld32(tS + 32 * i, s + 32 * i);
       tc_wait_ld();
+      if constexpr (C::kSepP) {  // S_t may be overwritten by S_t(j+1) now
+        tc_fence_before();
+        mbar_arrive(&bars->s_free[t]);
+      }
       const int key0 = j * kBN;
       if (key0 + kBN > Nk || (CAUSAL && key0 + kBN - 1 > tile_row0)) {
         const int lim = CAUSAL ? min(Nk, row + 1) : Nk;  // keys [key0, lim) are visible
@@ -261,38 +319,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kBN; ++i)
           if (key0 + i >= lim) s[i] = __float_as_uint(-INFINITY);
       }
-      // level 1: tile max (one thread owns the whole row)
-      float mx = __uint_as_float(s[0]);
+      // level 1: tile max over the row, four independent 3-input max chains
+      float mx4[4];
 #pragma unroll
-      for (int i = 1; i < kBN; ++i) mx = fmaxf(mx, __uint_as_float(s[i]));
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const uint32_t* sq = s + 32 * q4;
+        float m = max3f(__uint_as_float(sq[0]), __uint_as_float(sq[1]), __uint_as_float(sq[2]));
+#pragma unroll
+        for (int i = 3; i + 1 < 32; i += 2) m = max3f(m, __uint_as_float(sq[i]), __uint_as_float(sq[i + 1]));
+        mx4[q4] = fmaxf(m, __uint_as_float(sq[31]));
+      }
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       const float mt = mx * sl2;
       const bool need = mt > m_run + kRescaleThreshold;
       const float m_new = need ? mt : m_run;
-      const float alpha = exp2f(m_run - m_new);
-      // level 2: P = exp(s - m) to TMEM (16-bit, over the S columns), running sum
-      float sum = 0.f;
+      const float alpha = ex2_ftz(m_run - m_new);
+      // level 2: P = 2^(s*sl2 - m) (16-bit, packed in registers), running sum in
+      // four packed accumulators; all exponentials run before any wait below
+      const uint64_t negm2 = f2pack(-m_new, -m_new);
+      uint64_t sum2[4];
 #pragma unroll
-      for (int cc = 0; cc < kBN / 16; ++cc) {
-        uint32_t pk[8];
+      for (int q4 = 0; q4 < 4; ++q4) sum2[q4] = f2pack(0.f, 0.f);
+      uint32_t pk[kBN / 2];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float p0 = exp2f(fmaf(__uint_as_float(s[16 * cc + 2 * e]), sl2, -m_new));
-          const float p1 = exp2f(fmaf(__uint_as_float(s[16 * cc + 2 * e + 1]), sl2, -m_new));
-          sum += p0 + p1;
-          pk[e] = Pack<DT>::pack2(p0, p1);
-        }
-        tc_st8(tS + 8 * cc, pk);
+      for (int e = 0; e < kBN / 2; ++e) {
+        const uint64_t x = fma_f32x2(u2pack(s[2 * e], s[2 * e + 1]), sl2x2, negm2);
+        float x0, x1;
+        f2unpack(x, x0, x1);
+        const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
+        sum2[e & 3] = add_f32x2(sum2[e & 3], f2pack(p0, p1));
+        pk[e] = Pack<DT>::pack2(p0, p1);
       }
-      l_run = fmaf(l_run, alpha, sum);
+      if constexpr (C::kSepP) {  // PV_t(j-1) must be done before P_t and O_t are touched
+        if (j > 0) {
+          if (!(ok = warp_wait(&bars->pv_done[t], (j - 1) & 1))) break;
+          tc_fence_after();
+        }
+      }
+#pragma unroll
+      for (int cc = 0; cc < kBN / 16; ++cc) tc_st8(tP + 8 * cc, pk + 8 * cc);
+      const uint64_t sumv = add_f32x2(add_f32x2(sum2[0], sum2[1]), add_f32x2(sum2[2], sum2[3]));
+      float sum_lo, sum_hi;
+      f2unpack(sumv, sum_lo, sum_hi);
+      l_run = fmaf(l_run, alpha, sum_lo + sum_hi);
       // level 3 correction: rescale O in TMEM when some row's max moved
       if (j > 0 && __any_sync(0xffffffffu, need)) {
+        const uint64_t a2 = f2pack(alpha, alpha);
 #pragma unroll
         for (int i = 0; i < D / 32; ++i) {
           uint32_t ov[32];
           tc_ld32(tO + 32 * i, ov);
           tc_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+          for (int e = 0; e < 32; e += 2) {
+            const uint64_t r = mul_f32x2(u2pack(ov[e], ov[e + 1]), a2);
+            f2unpack_u(r, ov[e], ov[e + 1]);
+          }
           tc_st32(tO + 32 * i, ov);
         }
       }

@@ -12,6 +12,12 @@
 // normalisation, so x and the residual are read from HBM once and y is
 // written once.
 //
+// The kernel is bound by instruction issue as much as by HBM, so the
+// element-wise work runs on packed fp32 pairs (fma/add/mul .f32x2) and the
+// in-thread combine uses compile-time reciprocals.  The affine map keeps the
+// centred form y = (h - mean) * (gamma * rstd) + beta, so a constant row gives
+// exactly beta.
+//
 // Layout: a group of `tpr` threads (a multiple of 32) owns one row; thread t
 // holds the row's 16-byte vectors t, t + tpr, ..., t + (VPT-1)*tpr.  A CTA
 // holds max(1, 256 / tpr) rows.
@@ -24,13 +30,81 @@ struct Stats {
   float n, mean, m2;
 };
 
+// General pairwise combine (counts may differ or be zero).
 __device__ __forceinline__ Stats chan(Stats a, Stats b) {
   if (b.n == 0.f) return a;
   if (a.n == 0.f) return b;
   const float n = a.n + b.n;
-  const float f = b.n / n;
+  const float f = __fdividef(b.n, n);
   const float d = b.mean - a.mean;
   return Stats{n, fmaf(d, f, a.mean), a.m2 + b.m2 + d * d * a.n * f};
+}
+
+// 16-byte vector <-> packed fp32 pairs.
+template <Dt DT>
+struct Vec2;
+
+template <>
+struct Vec2<Dt::BF16> {
+  static constexpr int P = 4;  // pairs per 16 bytes
+  __device__ __forceinline__ static void unpack(const uint4& u, uint64_t* p) {
+    p[0] = u2pack(u.x << 16, u.x & 0xffff0000u);
+    p[1] = u2pack(u.y << 16, u.y & 0xffff0000u);
+    p[2] = u2pack(u.z << 16, u.z & 0xffff0000u);
+    p[3] = u2pack(u.w << 16, u.w & 0xffff0000u);
+  }
+  __device__ __forceinline__ static uint32_t pack1(uint64_t v) {
+    float lo, hi;
+    f2unpack(v, lo, hi);
+    return pack_bf16x2(lo, hi);
+  }
+  __device__ __forceinline__ static uint4 pack(const uint64_t* p) {
+    return make_uint4(pack1(p[0]), pack1(p[1]), pack1(p[2]), pack1(p[3]));
+  }
+};
+
+template <>
+struct Vec2<Dt::F16> {
+  static constexpr int P = 4;
+  __device__ __forceinline__ static uint64_t up1(uint32_t w) {
+    const float2 f = unpack_f16x2(w);
+    return f2pack(f.x, f.y);
+  }
+  __device__ __forceinline__ static void unpack(const uint4& u, uint64_t* p) {
+    p[0] = up1(u.x);
+    p[1] = up1(u.y);
+    p[2] = up1(u.z);
+    p[3] = up1(u.w);
+  }
+  __device__ __forceinline__ static uint32_t pack1(uint64_t v) {
+    float lo, hi;
+    f2unpack(v, lo, hi);
+    return pack_f16x2(lo, hi);
+  }
+  __device__ __forceinline__ static uint4 pack(const uint64_t* p) {
+    return make_uint4(pack1(p[0]), pack1(p[1]), pack1(p[2]), pack1(p[3]));
+  }
+};
+
+template <>
+struct Vec2<Dt::F32> {
+  static constexpr int P = 2;
+  __device__ __forceinline__ static void unpack(const uint4& u, uint64_t* p) {
+    p[0] = u2pack(u.x, u.y);
+    p[1] = u2pack(u.z, u.w);
+  }
+  __device__ __forceinline__ static uint4 pack(const uint64_t* p) {
+    uint4 u;
+    f2unpack_u(p[0], u.x, u.y);
+    f2unpack_u(p[1], u.z, u.w);
+    return u;
+  }
+};
+
+__device__ __forceinline__ float hsum(uint64_t v) {
+  float lo, hi;
+  f2unpack(v, lo, hi);
+  return lo + hi;
 }
 
 template <Dt DT, int VPT>
@@ -39,8 +113,9 @@ __global__ void __launch_bounds__(1024) ln_fused_kernel(const uint4* __restrict_
                                                         const uint4* __restrict__ beta, uint4* __restrict__ out,
                                                         uint4* __restrict__ r_out, int rows, int nvec, int tpr,
                                                         float inv_cols, float eps) {
-  using P = Pack<DT>;
-  constexpr int E = P::E;
+  using V = Vec2<DT>;
+  constexpr int P = V::P;
+  constexpr int E = 2 * P;  // elements per 16-byte vector
   __shared__ Stats s_warp[32];
 
   const int rows_per_cta = blockDim.x / tpr;
@@ -64,27 +139,42 @@ __global__ void __launch_bounds__(1024) ln_fused_kernel(const uint4* __restrict_
   }
 
   // Levels 1-2, incremental: fold each 16-byte block into the running stats.
-  float h[VPT][E];
+  // Valid blocks of a thread form a prefix (i < count), so block i joins a
+  // running count of E*i and the combine factor n_b/n is the constant 1/(i+1).
+  uint64_t h[VPT][P];
   Stats st{0.f, 0.f, 0.f};
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
-    float xf[E], rf_[E];
-    P::unpack(xv[i], xf);
-    P::unpack(rv[i], rf_);
-    float s = 0.f;
+    uint64_t xp[P], rp[P];
+    V::unpack(xv[i], xp);
+    V::unpack(rv[i], rp);
+    uint64_t s2 = 0;
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      h[i][e] = xf[e] + rf_[e];
-      s += h[i][e];
+    for (int k = 0; k < P; ++k) {
+      h[i][k] = add_f32x2(xp[k], rp[k]);
+      s2 = k == 0 ? h[i][0] : add_f32x2(s2, h[i][k]);
     }
-    const float mb = s * (1.0f / E);
-    float q = 0.f;
+    const float mb = hsum(s2) * (1.0f / E);
+    const uint64_t negmb = f2pack(-mb, -mb);
+    uint64_t q2 = 0;
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const float d = h[i][e] - mb;
-      q = fmaf(d, d, q);
+    for (int k = 0; k < P; ++k) {
+      const uint64_t d = add_f32x2(h[i][k], negmb);
+      q2 = k == 0 ? mul_f32x2(d, d) : fma_f32x2(d, d, q2);
     }
-    if (t + i * tpr < nvec) st = chan(st, Stats{float(E), mb, q});
+    const float q = hsum(q2);
+    if (t + i * tpr < nvec) {
+      if (i == 0) {
+        st = Stats{float(E), mb, q};
+      } else {
+        constexpr float kE = float(E);
+        const float f = 1.0f / float(i + 1);  // folded at compile time (unrolled i)
+        const float d = mb - st.mean;
+        st.mean = fmaf(d, f, st.mean);
+        st.m2 = st.m2 + q + d * d * (kE * i) * f;
+        st.n += kE;
+      }
+    }
   }
   // Merge the threads of the warp (all 32 lanes belong to this row).
 #pragma unroll
@@ -105,37 +195,41 @@ __global__ void __launch_bounds__(1024) ln_fused_kernel(const uint4* __restrict_
   }
   if (!row_ok) return;
 
-  // Level 3: normalise and apply the affine map from registers.
-  const float mean = st.mean;
+  // Level 3: y = (h - mean) * (gamma * rstd) + beta, three packed ops per pair.
   const float rstd = rsqrtf(st.m2 * inv_cols + eps);
+  const uint64_t rstd2 = f2pack(rstd, rstd), negmean2 = f2pack(-st.mean, -st.mean);
+  const uint64_t one2 = f2pack(1.f, 1.f), zero2 = 0;
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int c = t + i * tpr;
     if (c >= nvec) continue;
-    float g[E], b[E], y[E];
+    uint64_t g[P], b[P], y[P];
     if (gamma) {
-      P::unpack(__ldg(gamma + c), g);
+      V::unpack(__ldg(gamma + c), g);
     } else {
 #pragma unroll
-      for (int e = 0; e < E; ++e) g[e] = 1.f;
+      for (int k = 0; k < P; ++k) g[k] = one2;
     }
     if (beta) {
-      P::unpack(__ldg(beta + c), b);
+      V::unpack(__ldg(beta + c), b);
     } else {
 #pragma unroll
-      for (int e = 0; e < E; ++e) b[e] = 0.f;
+      for (int k = 0; k < P; ++k) b[k] = zero2;
     }
 #pragma unroll
-    for (int e = 0; e < E; ++e) y[e] = fmaf((h[i][e] - mean) * rstd, g[e], b[e]);
-    st_stream(out + base + c, P::pack(y));
-    if (r_out) st_stream(r_out + base + c, P::pack(h[i]));
+    for (int k = 0; k < P; ++k) {
+      const uint64_t a = mul_f32x2(g[k], rstd2);
+      y[k] = fma_f32x2(add_f32x2(h[i][k], negmean2), a, b[k]);
+    }
+    st_stream(out + base + c, V::pack(y));
+    if (r_out) st_stream(r_out + base + c, V::pack(h[i]));
   }
 }
 
 template <Dt DT>
 cudaError_t launch_dt(const void* x, const void* r, const void* g, const void* b, void* out, void* r_out,
                       int rows, int cols, float eps, cudaStream_t s) {
-  constexpr int E = Pack<DT>::E;
+  constexpr int E = 2 * Vec2<DT>::P;
   const int nvec = cols / E;
   const int vpt = nvec >= 256 ? 4 : (nvec >= 64 ? 2 : 1);
   int tpr = (nvec + vpt - 1) / vpt;
