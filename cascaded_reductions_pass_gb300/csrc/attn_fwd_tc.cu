@@ -18,8 +18,8 @@
 //   warps 4-7   softmax for query tile 0, warps 8-11 for tile 1: one thread
 //               per query row, i.e. per TMEM lane, so row max and row sum need
 //               no cross-thread reduction.
-// Registers are re-split after launch: warps 0-3 drop to 64 per thread and
-// the softmax warps rise to 216 (a row of S is 128 registers).
+// Registers are re-split after launch: warps 0-3 drop to 80 per thread and
+// the softmax warps rise to 208 (a row of S is 128 registers).
 //
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D).
 //  * D = 64: P0 [384,448) and P1 [448,512) have columns of their own (16-bit,
@@ -54,8 +54,8 @@ constexpr int kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // base-2 units
-constexpr int kRegsCtl = 64;       // per thread, warps 0-3 after reallocation
-constexpr int kRegsSoftmax = 216;  // per thread, warps 4-11 after reallocation
+constexpr int kRegsCtl = 80;       // per thread, warps 0-3 after reallocation
+constexpr int kRegsSoftmax = 208;  // per thread, warps 4-11 after reallocation
 
 template <int D>
 struct Cfg {
@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  // Register split: 128 x 64 (producer / MMA warpgroup) + 256 x 216 (softmax)
+  // Register split: 128 x 80 (producer / MMA warpgroup) + 256 x 208 (softmax)
   // = 63,488 <= 384 x 168 registers granted at launch.
   static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= kThreads * 168, "register split exceeds the launch budget");
   if (warp < 4) {
@@ -182,26 +182,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!drained) atomicOr(status, kStatusTimeout);
     } else if (warp == 1 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
-      const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK), va = smem_u32(sV);
+      // Issue cost matters here (one thread issues every MMA), so the shared
+      // memory descriptors are built once: a K-step or a ring stage only moves
+      // the 14-bit start-address field, i.e. adds a constant to the descriptor.
       constexpr uint32_t idS = tc_idesc_f16(kBF16, kBM, kBN, false);
       constexpr uint32_t idPV = tc_idesc_f16(kBF16, kBM, D, true);
-      auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T  (M=128, N=128, K=D)
-        const uint32_t qbase = qa + t * C::kQBytes, kbase = ka + (j % S) * C::kKVBytes;
+      const uint64_t dQ = tc_sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dK = tc_sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dV = tc_sdesc_sw128(smem_u32(sV), kBN * 128, 1024);
+      auto issue_s = [&](int t, int st) {  // S_t = Q_t K^T from K stage st  (M=128, N=128, K=D)
+        const uint64_t a0 = dQ + static_cast<uint64_t>(t * (C::kQBytes >> 4));
+        const uint64_t b0 = dK + static_cast<uint64_t>(st * (C::kKVBytes >> 4));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off_q = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-          const uint32_t off_k = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
-          tc_mma_ss(tmem + t * kBN, tc_sdesc_sw128(qbase + off_q, 16, 1024), tc_sdesc_sw128(kbase + off_k, 16, 1024),
-                    idS, kk > 0 ? 1u : 0u);
+          constexpr int kStepQ = kBM * 128 / 16, kStepK = kBN * 128 / 16;  // one 64-dim box
+          const uint32_t oq = (kk >> 2) * kStepQ + (kk & 3) * 2, ok_ = (kk >> 2) * kStepK + (kk & 3) * 2;
+          tc_mma_ss(tmem + t * kBN, a0 + oq, b0 + ok_, idS, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int t, int j) {  // O_t += P_t V_j  (M=128, N=D, K=128; P from TMEM)
-        const uint32_t vbase = va + (j % S) * C::kKVBytes;
-        const uint32_t pcol = C::kSepP ? C::kPCol + t * (kBN / 2) : t * kBN;
+      auto issue_pv = [&](int t, int st, bool acc) {  // O_t += P_t V from V stage st  (M=128, N=D, K=128)
+        const uint64_t b0 = dV + static_cast<uint64_t>(st * (C::kKVBytes >> 4));
+        const uint32_t pcol = tmem + (C::kSepP ? C::kPCol + t * (kBN / 2) : t * kBN);
+        const uint32_t dO = tmem + C::kOCol + t * D;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          tc_mma_ts(tmem + C::kOCol + t * D, tmem + pcol + kk * 8,
-                    tc_sdesc_sw128(vbase + kk * 16 * 128, kBN * 128, 1024), idPV, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_ts(dO, pcol + kk * 8, b0 + kk * (16 * 128 / 16), idPV, (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(&bars->q_full, 0) && mbar_wait(&bars->k_full[0], 0);
       if (ok) {
@@ -212,71 +217,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(&bars->s_full[1]);
         tc_commit(&bars->k_empty[0]);
       }
+      int st = 0, ph = 0;  // ring stage and phase of tile j
       for (int j = 0; ok && j < nt1; ++j) {
-        const int st = j % S, jn = j + 1, stn = jn % S;
+        const int jn = j + 1;
+        const int stn = st + 1 == S ? 0 : st + 1, phn = st + 1 == S ? ph ^ 1 : ph;  // stage / phase of j+1
         bool k_ready = false;
         if constexpr (C::kSepP) {
           // S_t(j+1) as soon as softmax t has read S_t(j); PV_t(j) once P_t(j) is ready.
           if (jn < nt0) {
-            if (!(ok = mbar_wait(&bars->s_free[0], j & 1) && mbar_wait(&bars->k_full[stn], (jn / S) & 1))) break;
+            if (!(ok = mbar_wait(&bars->s_free[0], j & 1) && mbar_wait(&bars->k_full[stn], phn))) break;
             k_ready = true;
             tc_fence_after();
-            issue_s(0, jn);
+            issue_s(0, stn);
             tc_commit(&bars->s_full[0]);
           }
-          if (!(ok = mbar_wait(&bars->v_full[st], (j / S) & 1))) break;
+          if (!(ok = mbar_wait(&bars->v_full[st], ph))) break;
           if (j < nt0) {
             if (!(ok = mbar_wait(&bars->p_ready[0], j & 1))) break;
             tc_fence_after();
-            issue_pv(0, j);
+            issue_pv(0, st, j > 0);
             tc_commit(&bars->pv_done[0]);
             if (j == nt0 - 1) tc_commit(&bars->o_final[0]);
           }
           if (jn < nt1) {
             if (!(ok = mbar_wait(&bars->s_free[1], j & 1))) break;
-            if (!k_ready && !(ok = mbar_wait(&bars->k_full[stn], (jn / S) & 1))) break;
+            if (!k_ready && !(ok = mbar_wait(&bars->k_full[stn], phn))) break;
             tc_fence_after();
-            issue_s(1, jn);
+            issue_s(1, stn);
             tc_commit(&bars->s_full[1]);
             tc_commit(&bars->k_empty[stn]);
           }
           if (!(ok = mbar_wait(&bars->p_ready[1], j & 1))) break;
           tc_fence_after();
-          issue_pv(1, j);
+          issue_pv(1, st, j > 0);
           tc_commit(&bars->pv_done[1]);
           tc_commit(&bars->v_empty[st]);
           if (j == nt1 - 1) tc_commit(&bars->o_final[1]);
         } else {
           // P aliases S: PV_t(j) must be issued before S_t(j+1) overwrites it.
-          if (!(ok = mbar_wait(&bars->v_full[st], (j / S) & 1))) break;
+          if (!(ok = mbar_wait(&bars->v_full[st], ph))) break;
           if (j < nt0) {
             if (!(ok = mbar_wait(&bars->p_ready[0], j & 1))) break;
             tc_fence_after();
-            issue_pv(0, j);
+            issue_pv(0, st, j > 0);
             if (j == nt0 - 1) tc_commit(&bars->o_final[0]);
           }
           if (jn < nt0) {
-            if (!(ok = mbar_wait(&bars->k_full[stn], (jn / S) & 1))) break;
+            if (!(ok = mbar_wait(&bars->k_full[stn], phn))) break;
             k_ready = true;
             tc_fence_after();
-            issue_s(0, jn);
+            issue_s(0, stn);
             tc_commit(&bars->s_full[0]);
           }
           if (!(ok = mbar_wait(&bars->p_ready[1], j & 1))) break;
           tc_fence_after();
-          issue_pv(1, j);
+          issue_pv(1, st, j > 0);
           if (j == nt1 - 1) tc_commit(&bars->o_final[1]);
           tc_commit(&bars->v_empty[st]);
           if (jn < nt1) {
             if (!k_ready) {
-              if (!(ok = mbar_wait(&bars->k_full[stn], (jn / S) & 1))) break;
+              if (!(ok = mbar_wait(&bars->k_full[stn], phn))) break;
               tc_fence_after();
             }
-            issue_s(1, jn);
+            issue_s(1, stn);
             tc_commit(&bars->s_full[1]);
             tc_commit(&bars->k_empty[stn]);
           }
         }
+        st = stn;
+        ph = phn;
       }
       if (!ok) {
         atomicOr(status, kStatusTimeout);
