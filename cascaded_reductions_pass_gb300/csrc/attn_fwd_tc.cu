@@ -14,7 +14,10 @@
 // CTA = two query tiles of 128 rows (rows r0..r0+255 of one (batch, head)),
 // 12 warps:
 //   warp 0      TMA producer: Q once; K and V tiles through 2-3 stage rings.
-//   warp 1      allocates 512 TMEM columns; lane 0 issues every tcgen05.mma.
+//   warp 1      allocates 512 TMEM columns and issues every tcgen05.mma.
+// Both run their loops as a whole warp with warp-uniform operands; one lane
+// issues through an elect.sync predicate (no divergent branch), which keeps
+// the issue cost at the tensor core's own rate.
 //   warps 4-7   softmax for query tile 0, warps 8-11 for tile 1: one thread
 //               per query row, i.e. per TMEM lane, so row max and row sum need
 //               no cross-thread reduction.
@@ -141,50 +144,51 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= kThreads * 168, "register split exceeds the launch budget");
   if (warp < 4) {
     regs_dec<kRegsCtl>();
-    if (warp == 0 && lane == 0) {
-      // ---------------------------------------------------------- TMA producer
+    if (warp == 0) {
+      // ---------------------------------------------------------- TMA producer (whole warp, one lane issues)
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
-      mbar_expect_tx(&bars->q_full, 2 * C::kQBytes);
+      mbar_expect_tx_elect(&bars->q_full, 2 * C::kQBytes);
 #pragma unroll
       for (int t = 0; t < 2; ++t)
 #pragma unroll
         for (int bx = 0; bx < D / 64; ++bx)
-          tma_load_3d(sQ + t * C::kQBytes + bx * (kBM * 128), &tq, &bars->q_full, bx * 64, r0 + t * kBM, bh);
+          tma_load_3d_elect(sQ + t * C::kQBytes + bx * (kBM * 128), &tq, &bars->q_full, bx * 64, r0 + t * kBM, bh);
       int issued_k = 0, issued_v = 0;
       bool ok = true;
       for (int j = 0; j < nt1; ++j) {
         const int st = j % S;
-        if (j >= S && !(ok = mbar_wait(&bars->k_empty[st], ((j / S) - 1) & 1))) break;
-        mbar_expect_tx(&bars->k_full[st], C::kKVBytes);
+        if (j >= S && !(ok = mbar_wait_warp(&bars->k_empty[st], ((j / S) - 1) & 1))) break;
+        mbar_expect_tx_elect(&bars->k_full[st], C::kKVBytes);
 #pragma unroll
         for (int bx = 0; bx < D / 64; ++bx)
-          tma_load_3d(sK + st * C::kKVBytes + bx * (kBN * 128), &tk, &bars->k_full[st], bx * 64, j * kBN, kv_plane);
+          tma_load_3d_elect(sK + st * C::kKVBytes + bx * (kBN * 128), &tk, &bars->k_full[st], bx * 64, j * kBN, kv_plane);
         ++issued_k;
-        if (j >= S && !(ok = mbar_wait(&bars->v_empty[st], ((j / S) - 1) & 1))) break;
-        mbar_expect_tx(&bars->v_full[st], C::kKVBytes);
+        if (j >= S && !(ok = mbar_wait_warp(&bars->v_empty[st], ((j / S) - 1) & 1))) break;
+        mbar_expect_tx_elect(&bars->v_full[st], C::kKVBytes);
 #pragma unroll
         for (int bx = 0; bx < D / 64; ++bx)
-          tma_load_3d(sV + st * C::kKVBytes + bx * (kBN * 128), &tv, &bars->v_full[st], bx * 64, j * kBN, kv_plane);
+          tma_load_3d_elect(sV + st * C::kKVBytes + bx * (kBN * 128), &tv, &bars->v_full[st], bx * 64, j * kBN, kv_plane);
         ++issued_v;
       }
       if (!ok) {
-        atomicOr(status, kStatusTimeout);
+        if (lane == 0) atomicOr(status, kStatusTimeout);
         bars->abort = 1;
       }
       // every copy issued must land before the CTA exits
-      bool drained = mbar_wait(&bars->q_full, 0);
+      bool drained = mbar_wait_warp(&bars->q_full, 0);
       for (int j = issued_k > S ? issued_k - S : 0; j < issued_k; ++j)
-        drained &= mbar_wait(&bars->k_full[j % S], (j / S) & 1);
+        drained &= mbar_wait_warp(&bars->k_full[j % S], (j / S) & 1);
       for (int j = issued_v > S ? issued_v - S : 0; j < issued_v; ++j)
-        drained &= mbar_wait(&bars->v_full[j % S], (j / S) & 1);
-      if (!drained) atomicOr(status, kStatusTimeout);
-    } else if (warp == 1 && lane == 0) {
-      // ---------------------------------------------------------- MMA issuer
-      // Issue cost matters here (one thread issues every MMA), so the shared
-      // memory descriptors are built once: a K-step or a ring stage only moves
-      // the 14-bit start-address field, i.e. adds a constant to the descriptor.
+        drained &= mbar_wait_warp(&bars->v_full[j % S], (j / S) & 1);
+      if (!drained && lane == 0) atomicOr(status, kStatusTimeout);
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer (whole warp, one lane issues)
+      // Issue cost matters here (one lane issues every MMA), so the whole warp
+      // runs this loop with warp-uniform operands and elect.sync predicates the
+      // instructions; the shared memory descriptors are built once: a K-step or
+      // a ring stage only moves the 14-bit start-address field.
       constexpr uint32_t idS = tc_idesc_f16(kBF16, kBM, kBN, false);
       constexpr uint32_t idPV = tc_idesc_f16(kBF16, kBM, D, true);
       const uint64_t dQ = tc_sdesc_sw128(smem_u32(sQ), 16, 1024);
@@ -197,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk) {
           constexpr int kStepQ = kBM * 128 / 16, kStepK = kBN * 128 / 16;  // one 64-dim box
           const uint32_t oq = (kk >> 2) * kStepQ + (kk & 3) * 2, ok_ = (kk >> 2) * kStepK + (kk & 3) * 2;
-          tc_mma_ss(tmem + t * kBN, a0 + oq, b0 + ok_, idS, kk > 0 ? 1u : 0u);
+          tc_mma_ss_elect(tmem + t * kBN, a0 + oq, b0 + ok_, idS, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int t, int st, bool acc) {  // O_t += P_t V from V stage st  (M=128, N=D, K=128)
@@ -206,16 +210,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t dO = tmem + C::kOCol + t * D;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          tc_mma_ts(dO, pcol + kk * 8, b0 + kk * (16 * 128 / 16), idPV, (acc || kk > 0) ? 1u : 0u);
+          tc_mma_ts_elect(dO, pcol + kk * 8, b0 + kk * (16 * 128 / 16), idPV, (acc || kk > 0) ? 1u : 0u);
       };
-      bool ok = mbar_wait(&bars->q_full, 0) && mbar_wait(&bars->k_full[0], 0);
+      bool ok = mbar_wait_warp(&bars->q_full, 0) && mbar_wait_warp(&bars->k_full[0], 0);
       if (ok) {
         tc_fence_after();
         issue_s(0, 0);
-        tc_commit(&bars->s_full[0]);
+        tc_commit_elect(&bars->s_full[0]);
         issue_s(1, 0);
-        tc_commit(&bars->s_full[1]);
-        tc_commit(&bars->k_empty[0]);
+        tc_commit_elect(&bars->s_full[1]);
+        tc_commit_elect(&bars->k_empty[0]);
       }
       int st = 0, ph = 0;  // ring stage and phase of tile j
       for (int j = 0; ok && j < nt1; ++j) {
@@ -225,75 +229,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (C::kSepP) {
           // S_t(j+1) as soon as softmax t has read S_t(j); PV_t(j) once P_t(j) is ready.
           if (jn < nt0) {
-            if (!(ok = mbar_wait(&bars->s_free[0], j & 1) && mbar_wait(&bars->k_full[stn], phn))) break;
+            if (!(ok = mbar_wait_warp(&bars->s_free[0], j & 1) && mbar_wait_warp(&bars->k_full[stn], phn))) break;
             k_ready = true;
             tc_fence_after();
             issue_s(0, stn);
-            tc_commit(&bars->s_full[0]);
+            tc_commit_elect(&bars->s_full[0]);
           }
-          if (!(ok = mbar_wait(&bars->v_full[st], ph))) break;
+          if (!(ok = mbar_wait_warp(&bars->v_full[st], ph))) break;
           if (j < nt0) {
-            if (!(ok = mbar_wait(&bars->p_ready[0], j & 1))) break;
+            if (!(ok = mbar_wait_warp(&bars->p_ready[0], j & 1))) break;
             tc_fence_after();
             issue_pv(0, st, j > 0);
-            tc_commit(&bars->pv_done[0]);
-            if (j == nt0 - 1) tc_commit(&bars->o_final[0]);
+            tc_commit_elect(&bars->pv_done[0]);
+            if (j == nt0 - 1) tc_commit_elect(&bars->o_final[0]);
           }
           if (jn < nt1) {
-            if (!(ok = mbar_wait(&bars->s_free[1], j & 1))) break;
-            if (!k_ready && !(ok = mbar_wait(&bars->k_full[stn], phn))) break;
+            if (!(ok = mbar_wait_warp(&bars->s_free[1], j & 1))) break;
+            if (!k_ready && !(ok = mbar_wait_warp(&bars->k_full[stn], phn))) break;
             tc_fence_after();
             issue_s(1, stn);
-            tc_commit(&bars->s_full[1]);
-            tc_commit(&bars->k_empty[stn]);
+            tc_commit_elect(&bars->s_full[1]);
+            tc_commit_elect(&bars->k_empty[stn]);
           }
-          if (!(ok = mbar_wait(&bars->p_ready[1], j & 1))) break;
+          if (!(ok = mbar_wait_warp(&bars->p_ready[1], j & 1))) break;
           tc_fence_after();
           issue_pv(1, st, j > 0);
-          tc_commit(&bars->pv_done[1]);
-          tc_commit(&bars->v_empty[st]);
-          if (j == nt1 - 1) tc_commit(&bars->o_final[1]);
+          tc_commit_elect(&bars->pv_done[1]);
+          tc_commit_elect(&bars->v_empty[st]);
+          if (j == nt1 - 1) tc_commit_elect(&bars->o_final[1]);
         } else {
           // P aliases S: PV_t(j) must be issued before S_t(j+1) overwrites it.
-          if (!(ok = mbar_wait(&bars->v_full[st], ph))) break;
+          if (!(ok = mbar_wait_warp(&bars->v_full[st], ph))) break;
           if (j < nt0) {
-            if (!(ok = mbar_wait(&bars->p_ready[0], j & 1))) break;
+            if (!(ok = mbar_wait_warp(&bars->p_ready[0], j & 1))) break;
             tc_fence_after();
             issue_pv(0, st, j > 0);
-            if (j == nt0 - 1) tc_commit(&bars->o_final[0]);
+            if (j == nt0 - 1) tc_commit_elect(&bars->o_final[0]);
           }
           if (jn < nt0) {
-            if (!(ok = mbar_wait(&bars->k_full[stn], phn))) break;
+            if (!(ok = mbar_wait_warp(&bars->k_full[stn], phn))) break;
             k_ready = true;
             tc_fence_after();
             issue_s(0, stn);
-            tc_commit(&bars->s_full[0]);
+            tc_commit_elect(&bars->s_full[0]);
           }
-          if (!(ok = mbar_wait(&bars->p_ready[1], j & 1))) break;
+          if (!(ok = mbar_wait_warp(&bars->p_ready[1], j & 1))) break;
           tc_fence_after();
           issue_pv(1, st, j > 0);
-          if (j == nt1 - 1) tc_commit(&bars->o_final[1]);
-          tc_commit(&bars->v_empty[st]);
+          if (j == nt1 - 1) tc_commit_elect(&bars->o_final[1]);
+          tc_commit_elect(&bars->v_empty[st]);
           if (jn < nt1) {
             if (!k_ready) {
-              if (!(ok = mbar_wait(&bars->k_full[stn], phn))) break;
+              if (!(ok = mbar_wait_warp(&bars->k_full[stn], phn))) break;
               tc_fence_after();
             }
             issue_s(1, stn);
-            tc_commit(&bars->s_full[1]);
-            tc_commit(&bars->k_empty[stn]);
+            tc_commit_elect(&bars->s_full[1]);
+            tc_commit_elect(&bars->k_empty[stn]);
           }
         }
         st = stn;
         ph = phn;
       }
       if (!ok) {
-        atomicOr(status, kStatusTimeout);
+        if (lane == 0) atomicOr(status, kStatusTimeout);
         bars->abort = 1;
       }
       // every MMA issued must complete before TMEM is released
-      tc_commit(&bars->drain);
-      if (!mbar_wait(&bars->drain, 0)) atomicOr(status, kStatusTimeout);
+      tc_commit_elect(&bars->drain);
+      if (!mbar_wait_warp(&bars->drain, 0) && lane == 0) atomicOr(status, kStatusTimeout);
     }
   } else {
     regs_inc<kRegsSoftmax>();
