@@ -130,7 +130,7 @@ class Runner:
         self.rf = rf
         self.w = inputs.WORKLOADS[name]
         if batch:  # a smaller case of the same kernel (for profiler captures)
-            key = "rows" if self.w.kind == "layernorm" else "B"
+            key = "rows" if self.w.kind in ("layernorm", "rmsnorm", "xent") else "B"
             self.w = dataclasses.replace(self.w, dims={**self.w.dims, key: int(batch)})
         self.dev = dev
         d = self.w.dims
@@ -153,6 +153,18 @@ class Runner:
             self.metric, self.unit, self.bound = "split-KV decode GB/s", "GB/s", "hbm"
             self.units = self.bytes / 1e9
             self.kernel_file, self.kernel = "decode_split.cu", "decode_split (+ lse_merge)"
+        elif self.w.kind == "xent":
+            self.bytes = workmodel.xent_bytes(d["rows"], d["vocab"], self.dtype)
+            self.flops = 4.0 * d["rows"] * d["vocab"]
+            self.metric, self.unit, self.bound = "softmax cross-entropy GB/s", "GB/s", "hbm"
+            self.units = self.bytes / 1e9
+            self.kernel_file, self.kernel = "xent_fused.cu", "xent"
+        elif self.w.kind == "rmsnorm":
+            self.bytes = workmodel.layernorm_bytes(d["rows"], d["cols"], self.dtype, affine=False) + d["cols"] * 2
+            self.flops = 4.0 * d["rows"] * d["cols"]
+            self.metric, self.unit, self.bound = "residual+RMSNorm GB/s", "GB/s", "hbm"
+            self.units = self.bytes / 1e9
+            self.kernel_file, self.kernel = "ln_fused.cu", "rms_fused"
         else:
             self.bytes = workmodel.layernorm_bytes(d["rows"], d["cols"], self.dtype)
             self.flops = 10.0 * d["rows"] * d["cols"]
@@ -168,6 +180,10 @@ class Runner:
             q = self.dev_in[0]
             self.o = torch.empty_like(q)
             self.lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+            self.outs = [self.o, self.lse]
+        elif self.w.kind == "xent":
+            self.o = torch.empty(d["rows"], dtype=torch.float32, device=dev)
+            self.lse = torch.empty(d["rows"], dtype=torch.float32, device=dev)
             self.outs = [self.o, self.lse]
         elif self.w.kind == "decode":
             q = self.dev_in[0]
@@ -187,6 +203,10 @@ class Runner:
         elif self.w.kind == "decode":
             rf.rf_attn_decode_splitkv(ins[0], ins[1], ins[2], self.o, self.ws, d["splits"], lse=self.lse,
                                       scale=self.scale)
+        elif self.w.kind == "rmsnorm":
+            rf.rf_rmsnorm_fused(ins[0], ins[1], ins[2], self.o, eps=d["eps"])
+        elif self.w.kind == "xent":
+            rf.rf_softmax_xent(ins[0], ins[1], self.o, self.lse)
         else:
             rf.rf_layernorm_fused(ins[0], ins[1], ins[2], ins[3], self.o, eps=d["eps"])
 
@@ -281,6 +301,22 @@ def oracle_sample(w, host, budget_s=12.0):
                 done_units += workmodel.decode_bytes(1, G, 1, d["L"], d["D"], w.dtype) / 1e9
                 groups += 1
         what = f"{groups} (batch, kv-head) groups of {G} query heads over all {d['L']} keys"
+    elif w.kind == "xent":
+        z, t = host
+        rows = 0
+        while rows < d["rows"] and (rows == 0 or time.perf_counter() - t_start < budget_s):
+            oracle.softmax_xent(z[rows:rows + 64], t[rows:rows + 64])
+            rows += 64
+        done_units = workmodel.xent_bytes(rows, d["vocab"], w.dtype) / 1e9
+        what = f"the first {rows} of {d['rows']} rows"
+    elif w.kind == "rmsnorm":
+        x, r, g = host
+        rows = 0
+        while rows < d["rows"] and (rows == 0 or time.perf_counter() - t_start < budget_s):
+            oracle.rmsnorm(x[rows:rows + 512], r[rows:rows + 512], g, d["eps"])
+            rows += 512
+        done_units = (workmodel.layernorm_bytes(rows, d["cols"], w.dtype, affine=False) + d["cols"] * 2) / 1e9
+        what = f"the first {rows} of {d['rows']} rows"
     else:
         x, r, g, b = host
         rows = 0
@@ -378,7 +414,7 @@ def main():
             if i >= args.warmup:
                 per_step.append((v, secs))
         val = float(np.mean([v for v, _ in per_step]))
-        unit = "TFLOP/s" if w.kind == "attn" else "GB/s"
+        unit = "TFLOP/s" if w.kind == "attn" else "GB/s"  # decode, layernorm, rmsnorm: GB/s
         ms = float(np.mean([s for _, s in per_step]) * 1e3)
         print(json.dumps({
             "impl": "reference", "metric": "fused cascaded-reduction throughput (CPU fp64 oracle)", "value": val,

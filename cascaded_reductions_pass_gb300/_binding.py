@@ -37,6 +37,8 @@ _SIGNATURES = {
     "rf_attn_decode_splitkv_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp], _i),
     "rf_lse_merge": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp], _i),
     "rf_layernorm_fused": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _f, _i, _vp], _i),
+    "rf_rmsnorm_fused": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _f, _i, _vp], _i),
+    "rf_softmax_xent": ([_vp, _vp, _vp, _vp, _vp, _i, _i, ctypes.c_longlong, _i, _vp], _i),
     "rf_last_error": ([], ctypes.c_char_p),
     "rf_version": ([], _i),
     "rf_device_status": ([_vp, _i], _i),
@@ -208,6 +210,35 @@ def rf_layernorm_fused(x, residual, gamma, beta, out, eps=1e-5, residual_out=Non
                                      _code(x.dtype), _stream(stream)))
 
 
+def rf_rmsnorm_fused(x, residual, gamma, out, eps=1e-5, residual_out=None, stream=None):
+    """out[rows,cols] <- RMSNorm(x + residual) * gamma (residual/gamma/residual_out may be None)."""
+    rows, cols = x.shape
+    for name, t in (("residual", residual), ("out", out), ("residual_out", residual_out)):
+        if t is not None and (tuple(t.shape) != (rows, cols) or t.dtype != x.dtype):
+            raise ValueError(f"{name} must match x")
+    if gamma is not None and (gamma.numel() != cols or gamma.dtype != x.dtype):
+        raise ValueError("gamma must hold cols elements of x's dtype")
+    _check(load().rf_rmsnorm_fused(_dev(x, "x"), _dev(residual, "residual", True), _dev(gamma, "gamma", True),
+                                   _dev(out, "out"), _dev(residual_out, "residual_out", True), rows, cols,
+                                   float(eps), _code(x.dtype), _stream(stream)))
+
+
+def rf_softmax_xent(logits, targets, loss, lse=None, grad=None, ignore_index=-100, stream=None):
+    """loss[rows] (and lse[rows], grad[rows,V]) <- cross-entropy of logits[rows,V] at int64 targets[rows]."""
+    rows, V = logits.shape
+    if targets.dtype != torch.int64 or targets.numel() != rows:
+        raise ValueError("targets must be int64 with rows elements")
+    if loss.dtype != torch.float32 or loss.numel() != rows:
+        raise ValueError("loss must be float32 with rows elements")
+    if lse is not None and (lse.dtype != torch.float32 or lse.numel() != rows):
+        raise ValueError("lse must be float32 with rows elements")
+    if grad is not None and (tuple(grad.shape) != (rows, V) or grad.dtype != logits.dtype):
+        raise ValueError("grad must match logits")
+    _check(load().rf_softmax_xent(_dev(logits, "logits"), _dev(targets, "targets"), _dev(loss, "loss"),
+                                  _dev(lse, "lse", True), _dev(grad, "grad", True), rows, V, int(ignore_index),
+                                  _code(logits.dtype), _stream(stream)))
+
+
 # ------------------------------------------------------------------ allocating helpers
 def attention(q, k, v, scale=None, causal=False, stream=None):
     """Allocate (o, lse) and run rf_attn_fwd."""
@@ -242,6 +273,22 @@ def decode_partials_view(workspace, B, Hq, D, num_splits):
     return o_part, lse_part
 
 
+def rmsnorm(x, residual, gamma, eps=1e-5, want_residual_out=False, stream=None):
+    out = torch.empty_like(x)
+    rout = torch.empty_like(x) if want_residual_out else None
+    rf_rmsnorm_fused(x, residual, gamma, out, eps=eps, residual_out=rout, stream=stream)
+    return (out, rout) if want_residual_out else out
+
+
+def softmax_xent(logits, targets, ignore_index=-100, want_grad=False, stream=None):
+    rows = logits.shape[0]
+    loss = torch.empty(rows, dtype=torch.float32, device=logits.device)
+    lse = torch.empty(rows, dtype=torch.float32, device=logits.device)
+    grad = torch.empty_like(logits) if want_grad else None
+    rf_softmax_xent(logits, targets, loss, lse, grad, ignore_index=ignore_index, stream=stream)
+    return (loss, lse, grad) if want_grad else (loss, lse)
+
+
 def layernorm(x, residual, gamma, beta, eps=1e-5, want_residual_out=False, stream=None):
     out = torch.empty_like(x)
     rout = torch.empty_like(x) if want_residual_out else None
@@ -252,7 +299,7 @@ def layernorm(x, residual, gamma, beta, eps=1e-5, want_residual_out=False, strea
 __all__ = [
     "RFError", "load", "declared_symbols", "rf_version", "rf_last_error", "rf_device_status", "rf_attn_fwd",
     "rf_attn_decode_splitkv_workspace_bytes", "rf_attn_decode_splitkv", "rf_attn_decode_splitkv_noalloc",
-    "rf_lse_merge", "rf_layernorm_fused",
+    "rf_lse_merge", "rf_layernorm_fused", "rf_rmsnorm_fused", "rmsnorm", "rf_softmax_xent", "softmax_xent",
     "attention", "decode", "decode_workspace", "decode_partials_view", "layernorm",
     "RF_OK", "RF_ERR_INVALID_ARG", "RF_ERR_UNSUPPORTED", "RF_ERR_CUDA", "RF_ERR_TIMEOUT",
 ]

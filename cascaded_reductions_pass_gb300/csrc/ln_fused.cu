@@ -1,4 +1,5 @@
-// ln_fused.cu -- one-pass residual + LayerNorm ("Operator Fusion" guide,
+// ln_fused.cu -- one-pass residual + LayerNorm and residual + RMSNorm
+// ("Operator Fusion" guide,
 // section 1 traffic example and section 2 Pattern 2: mean -> variance ->
 // normalise; section 4 places eps inside the square root).
 //
@@ -226,7 +227,85 @@ __global__ void __launch_bounds__(1024) ln_fused_kernel(const uint4* __restrict_
   }
 }
 
-template <Dt DT>
+
+// RMSNorm: the one-level cascade sum(h^2) -> normalise.  Each thread folds its
+// 16-byte blocks into a running sum of squares (combine op +), the threads of
+// a row are summed by warp shuffles and then across warps in shared memory,
+// and y = h * (gamma * rsqrt(sum / n + eps)) is written from registers.
+template <Dt DT, int VPT>
+__global__ void __launch_bounds__(1024) rms_fused_kernel(const uint4* __restrict__ x, const uint4* __restrict__ r,
+                                                         const uint4* __restrict__ gamma, uint4* __restrict__ out,
+                                                         uint4* __restrict__ r_out, int rows, int nvec, int tpr,
+                                                         float inv_cols, float eps) {
+  using V = Vec2<DT>;
+  constexpr int P = V::P;
+  __shared__ float s_warp[32];
+
+  const int rows_per_cta = blockDim.x / tpr;
+  const int slot = threadIdx.x / tpr;
+  const int t = threadIdx.x - slot * tpr;
+  const long long row = static_cast<long long>(blockIdx.x) * rows_per_cta + slot;
+  const bool row_ok = row < rows;
+  const long long base = row * nvec;
+
+  uint4 xv[VPT], rv[VPT];
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int c = t + i * tpr;
+    xv[i] = make_uint4(0, 0, 0, 0);
+    rv[i] = make_uint4(0, 0, 0, 0);
+    if (row_ok && c < nvec) {
+      xv[i] = ld_stream(x + base + c);
+      if (r) rv[i] = ld_stream(r + base + c);
+    }
+  }
+  uint64_t h[VPT][P];
+  uint64_t q2 = 0;  // running sum of squares, two lanes of a packed pair
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    uint64_t xp[P], rp[P];
+    V::unpack(xv[i], xp);
+    V::unpack(rv[i], rp);
+#pragma unroll
+    for (int k = 0; k < P; ++k) {
+      h[i][k] = add_f32x2(xp[k], rp[k]);
+      q2 = fma_f32x2(h[i][k], h[i][k], q2);  // blocks past the row end are zero
+    }
+  }
+  float ss = hsum(q2);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const int warps_per_row = tpr >> 5;
+  if (warps_per_row > 1) {
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) s_warp[w] = ss;
+    __syncthreads();
+    const int w0 = slot * warps_per_row;
+    ss = s_warp[w0];
+    for (int j = 1; j < warps_per_row; ++j) ss += s_warp[w0 + j];
+  }
+  if (!row_ok) return;
+  const float rstd = rsqrtf(ss * inv_cols + eps);
+  const uint64_t rstd2 = f2pack(rstd, rstd);
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int c = t + i * tpr;
+    if (c >= nvec) continue;
+    uint64_t g[P], y[P];
+    if (gamma) {
+      V::unpack(__ldg(gamma + c), g);
+    } else {
+#pragma unroll
+      for (int k = 0; k < P; ++k) g[k] = f2pack(1.f, 1.f);
+    }
+#pragma unroll
+    for (int k = 0; k < P; ++k) y[k] = mul_f32x2(h[i][k], mul_f32x2(g[k], rstd2));
+    st_stream(out + base + c, V::pack(y));
+    if (r_out) st_stream(r_out + base + c, V::pack(h[i]));
+  }
+}
+
+template <Dt DT, bool RMS>
 cudaError_t launch_dt(const void* x, const void* r, const void* g, const void* b, void* out, void* r_out,
                       int rows, int cols, float eps, cudaStream_t s) {
   constexpr int E = 2 * Vec2<DT>::P;
@@ -245,12 +324,22 @@ cudaError_t launch_dt(const void* x, const void* r, const void* g, const void* b
   auto Bt = static_cast<const uint4*>(b);
   auto O = static_cast<uint4*>(out);
   auto RO = static_cast<uint4*>(r_out);
-  if (vpt == 4)
-    ln_fused_kernel<DT, 4><<<unsigned(grid), threads, 0, s>>>(X, R, G, Bt, O, RO, rows, nvec, tpr, inv_cols, eps);
-  else if (vpt == 2)
-    ln_fused_kernel<DT, 2><<<unsigned(grid), threads, 0, s>>>(X, R, G, Bt, O, RO, rows, nvec, tpr, inv_cols, eps);
-  else
-    ln_fused_kernel<DT, 1><<<unsigned(grid), threads, 0, s>>>(X, R, G, Bt, O, RO, rows, nvec, tpr, inv_cols, eps);
+  const unsigned gr = static_cast<unsigned>(grid);
+  if constexpr (RMS) {
+    if (vpt == 4)
+      rms_fused_kernel<DT, 4><<<gr, threads, 0, s>>>(X, R, G, O, RO, rows, nvec, tpr, inv_cols, eps);
+    else if (vpt == 2)
+      rms_fused_kernel<DT, 2><<<gr, threads, 0, s>>>(X, R, G, O, RO, rows, nvec, tpr, inv_cols, eps);
+    else
+      rms_fused_kernel<DT, 1><<<gr, threads, 0, s>>>(X, R, G, O, RO, rows, nvec, tpr, inv_cols, eps);
+  } else {
+    if (vpt == 4)
+      ln_fused_kernel<DT, 4><<<gr, threads, 0, s>>>(X, R, G, Bt, O, RO, rows, nvec, tpr, inv_cols, eps);
+    else if (vpt == 2)
+      ln_fused_kernel<DT, 2><<<gr, threads, 0, s>>>(X, R, G, Bt, O, RO, rows, nvec, tpr, inv_cols, eps);
+    else
+      ln_fused_kernel<DT, 1><<<gr, threads, 0, s>>>(X, R, G, Bt, O, RO, rows, nvec, tpr, inv_cols, eps);
+  }
   return cudaGetLastError();
 }
 
@@ -262,9 +351,19 @@ int layernorm_max_cols(Dt dt) { return 1024 * 4 * (dt == Dt::F32 ? 4 : 8); }
 cudaError_t launch_layernorm(const void* x, const void* r, const void* gamma, const void* beta, void* out,
                              void* r_out, int rows, int cols, float eps, Dt dt, cudaStream_t s) {
   switch (dt) {
-    case Dt::F32: return launch_dt<Dt::F32>(x, r, gamma, beta, out, r_out, rows, cols, eps, s);
-    case Dt::F16: return launch_dt<Dt::F16>(x, r, gamma, beta, out, r_out, rows, cols, eps, s);
-    case Dt::BF16: return launch_dt<Dt::BF16>(x, r, gamma, beta, out, r_out, rows, cols, eps, s);
+    case Dt::F32: return launch_dt<Dt::F32, false>(x, r, gamma, beta, out, r_out, rows, cols, eps, s);
+    case Dt::F16: return launch_dt<Dt::F16, false>(x, r, gamma, beta, out, r_out, rows, cols, eps, s);
+    case Dt::BF16: return launch_dt<Dt::BF16, false>(x, r, gamma, beta, out, r_out, rows, cols, eps, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_rmsnorm(const void* x, const void* r, const void* gamma, void* out, void* r_out, int rows, int cols,
+                           float eps, Dt dt, cudaStream_t s) {
+  switch (dt) {
+    case Dt::F32: return launch_dt<Dt::F32, true>(x, r, gamma, nullptr, out, r_out, rows, cols, eps, s);
+    case Dt::F16: return launch_dt<Dt::F16, true>(x, r, gamma, nullptr, out, r_out, rows, cols, eps, s);
+    case Dt::BF16: return launch_dt<Dt::BF16, true>(x, r, gamma, nullptr, out, r_out, rows, cols, eps, s);
   }
   return cudaErrorInvalidValue;
 }

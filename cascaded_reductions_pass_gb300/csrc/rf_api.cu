@@ -312,6 +312,54 @@ rf_status_t rf_layernorm_fused(const void* x, const void* residual, const void* 
                   "rf_layernorm_fused");
 }
 
+rf_status_t rf_softmax_xent(const void* logits, const long long* targets, float* loss, float* lse, void* grad,
+                            int rows, int vocab, long long ignore_index, rf_dtype_t dtype, void* stream) {
+  if (!logits || !targets || !loss)
+    return fail(RF_ERR_INVALID_ARG, "rf_softmax_xent: logits, targets and loss must be non-null");
+  if (rows <= 0 || vocab <= 0) return fail(RF_ERR_INVALID_ARG, "rf_softmax_xent: sizes must be positive");
+  if (!valid_dtype(dtype)) return fail(RF_ERR_INVALID_ARG, "rf_softmax_xent: unknown dtype %d", int(dtype));
+  if (!aligned16(logits) || !aligned16(grad))
+    return fail(RF_ERR_INVALID_ARG, "rf_softmax_xent: logits and grad must be 16-byte aligned");
+  const int vec = dtype == RF_F32 ? 4 : 8;
+  if (vocab % vec != 0)
+    return fail(RF_ERR_INVALID_ARG, "rf_softmax_xent: vocab=%d must be a multiple of %d for %s", vocab, vec,
+                dt_name(dtype));
+  RF_TRY(check_dev_ptr(logits, "logits"));
+  RF_TRY(check_dev_ptr(targets, "targets"));
+  RF_TRY(check_dev_ptr(loss, "loss"));
+  RF_TRY(check_dev_ptr(lse, "lse"));
+  RF_TRY(check_dev_ptr(grad, "grad"));
+  return launched(rf::launch_xent(logits, targets, loss, lse, grad, rows, vocab, ignore_index,
+                                  static_cast<rf::Dt>(dtype), static_cast<cudaStream_t>(stream)),
+                  "rf_softmax_xent");
+}
+
+rf_status_t rf_rmsnorm_fused(const void* x, const void* residual, const void* gamma, void* out, void* residual_out,
+                             int rows, int cols, float eps, rf_dtype_t dtype, void* stream) {
+  if (!x || !out) return fail(RF_ERR_INVALID_ARG, "rf_rmsnorm_fused: x and out must be non-null");
+  if (rows <= 0 || cols <= 0) return fail(RF_ERR_INVALID_ARG, "rf_rmsnorm_fused: sizes must be positive");
+  if (!(eps >= 0.0f) || !std::isfinite(eps))
+    return fail(RF_ERR_INVALID_ARG, "rf_rmsnorm_fused: eps must be finite and >= 0");
+  if (!valid_dtype(dtype)) return fail(RF_ERR_INVALID_ARG, "rf_rmsnorm_fused: unknown dtype %d", int(dtype));
+  if (!aligned16(x) || !aligned16(residual) || !aligned16(gamma) || !aligned16(out) || !aligned16(residual_out))
+    return fail(RF_ERR_INVALID_ARG, "rf_rmsnorm_fused: pointers must be 16-byte aligned");
+  const int vec = dtype == RF_F32 ? 4 : 8;
+  if (cols % vec != 0)
+    return fail(RF_ERR_INVALID_ARG, "rf_rmsnorm_fused: cols=%d must be a multiple of %d for %s", cols, vec,
+                dt_name(dtype));
+  if (cols > rf::layernorm_max_cols(static_cast<rf::Dt>(dtype)))
+    return fail(RF_ERR_UNSUPPORTED, "rf_rmsnorm_fused: cols=%d exceeds %d", cols,
+                rf::layernorm_max_cols(static_cast<rf::Dt>(dtype)));
+  RF_TRY(check_dev_ptr(x, "x"));
+  RF_TRY(check_dev_ptr(residual, "residual"));
+  RF_TRY(check_dev_ptr(gamma, "gamma"));
+  RF_TRY(check_dev_ptr(out, "out"));
+  RF_TRY(check_dev_ptr(residual_out, "residual_out"));
+  return launched(rf::launch_rmsnorm(x, residual, gamma, out, residual_out, rows, cols, eps,
+                                     static_cast<rf::Dt>(dtype), static_cast<cudaStream_t>(stream)),
+                  "rf_rmsnorm_fused");
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------

@@ -17,6 +17,14 @@ cudaError_t launch_layernorm(const void* x, const void* r, const void* gamma, co
                              void* out, void* r_out, int rows, int cols, float eps, Dt dt,
                              cudaStream_t s);
 
+// residual + RMSNorm (ln_fused.cu; same limits as LayerNorm)
+cudaError_t launch_rmsnorm(const void* x, const void* r, const void* gamma, void* out, void* r_out, int rows,
+                           int cols, float eps, Dt dt, cudaStream_t s);
+
+// softmax cross-entropy per row, optional gradient (xent_fused.cu)
+cudaError_t launch_xent(const void* logits, const long long* targets, float* loss, float* lse, void* grad, int rows,
+                        int vocab, long long ignore_index, Dt dt, cudaStream_t s);
+
 // log-sum-exp merge of split partials (lse_merge.cu)
 cudaError_t launch_lse_merge(const float* o_part, const float* lse_part, void* o, float* lse,
                              int rows, int splits, int D, Dt out_dt, cudaStream_t s);

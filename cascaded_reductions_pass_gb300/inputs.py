@@ -56,6 +56,15 @@ def ln_inputs(rows, cols, dtype, seed):
     return x, r, gamma, beta
 
 
+def xent_inputs(rows, vocab, dtype, seed, scale=2.0):
+    """logits [rows,vocab] ~ N(0, scale^2); targets [rows] int64 uniform in [0, vocab)."""
+    dt = DTYPES[dtype] if isinstance(dtype, str) else dtype
+    g = _gen(seed)
+    logits = _normal(g, (rows, vocab), dt, std=scale)
+    targets = torch.randint(0, vocab, (rows,), generator=g, dtype=torch.int64)
+    return logits, targets
+
+
 def merge_inputs(rows, num_splits, D, seed, empty_frac=0.0):
     """Arbitrary split partials: o_part [rows,S,D] ~ N(0,1), lse_part [rows,S] ~ 4*N(0,1).
 
@@ -92,7 +101,10 @@ class Workload:
 # attention (B=4 H=12 N=4096 D=64), a causal GQA bf16 attention (B=2 Hq=32
 # Hkv=8 N=8192 D=128), a split-KV decode on the Llama-3-70B head geometry
 # (batch 16, 64q/8kv heads, D=128, 32768 cached keys, 16 splits) and a
-# residual+LayerNorm over 16384 x 4096.
+# residual+LayerNorm over 16384 x 4096; and a residual+RMSNorm of the same
+# shape and a softmax cross-entropy over 4096 rows of a 128256-entry
+# vocabulary (the Llama-3 vocabulary size), the next workloads after the hot
+# path.
 WORKLOADS = {
     "attn_tiny_f32": Workload("attn_tiny_f32", "attn", "f32", 0,
                               dict(B=1, Hq=1, Hkv=1, N=128, D=64, causal=0)),
@@ -105,6 +117,10 @@ WORKLOADS = {
                                     dict(B=16, Hq=64, Hkv=8, L=32768, D=128, splits=16)),
     "layernorm_residual_bf16": Workload("layernorm_residual_bf16", "layernorm", "bf16", 4,
                                         dict(rows=16384, cols=4096, eps=1e-5)),
+    "rmsnorm_residual_bf16": Workload("rmsnorm_residual_bf16", "rmsnorm", "bf16", 6,
+                                      dict(rows=16384, cols=4096, eps=1e-5)),
+    "softmax_xent_bf16": Workload("softmax_xent_bf16", "xent", "bf16", 7,
+                                  dict(rows=4096, vocab=128256)),
 }
 
 
@@ -119,4 +135,9 @@ def make(workload: Workload):
                              workload.dtype, workload.seed)
     if workload.kind == "layernorm":
         return ln_inputs(d["rows"], d["cols"], workload.dtype, workload.seed)
+    if workload.kind == "rmsnorm":
+        x, r, g, _ = ln_inputs(d["rows"], d["cols"], workload.dtype, workload.seed)
+        return x, r, g
+    if workload.kind == "xent":
+        return xent_inputs(d["rows"], d["vocab"], workload.dtype, workload.seed)
     raise ValueError(workload.kind)

@@ -48,3 +48,8 @@ def layernorm_bytes(rows, cols, dtype, affine=True, residual_out=False):
     e = ELEM_BYTES[dtype]
     t = rows * cols * e
     return 3 * t + (t if residual_out else 0) + (2 * cols * e if affine else 0)
+
+
+def xent_bytes(rows, vocab, dtype, with_lse=True):
+    """Logits read once, int64 targets read, fp32 loss (and LSE) written once."""
+    return rows * vocab * ELEM_BYTES[dtype] + rows * 8 + rows * 4 + (rows * 4 if with_lse else 0)

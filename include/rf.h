@@ -201,6 +201,53 @@ rf_status_t rf_layernorm_fused(const void* x, const void* residual, const void* 
                                const void* beta, void* out, void* residual_out,
                                int rows, int cols, float eps, rf_dtype_t dtype, void* stream);
 
+/*
+ * rf_rmsnorm_fused -- residual add + RMSNorm in one pass over each row:
+ * h = x + residual; the one reduction level is the running sum of squares of
+ * h (combine op +); y = h * gamma / sqrt(sum(h^2)/cols + eps).  The
+ * "Operator Fusion" guide (section 3) lists RMSNorm with LayerNorm as a
+ * fusible reduction + normalise pattern; eps sits inside the root as in its
+ * LayerNorm kernels, and there is no bias.  The row stays on chip between
+ * the reduction and the normalisation (x and residual read once, y written
+ * once).
+ *
+ *   x, residual   [rows, cols] dtype (read; residual nullable)
+ *   gamma         [cols]       dtype (read; nullable = 1)
+ *   out           [rows, cols] dtype (written)
+ *   residual_out  [rows, cols] dtype, nullable (written: h rounded to dtype)
+ *
+ * Supported sizes, alignment and errors: as rf_layernorm_fused.
+ */
+rf_status_t rf_rmsnorm_fused(const void* x, const void* residual, const void* gamma, void* out,
+                             void* residual_out, int rows, int cols, float eps, rf_dtype_t dtype,
+                             void* stream);
+
+/*
+ * rf_softmax_xent -- fused softmax + cross-entropy per row of logits, the
+ * cascade max -> sum exp -> loss ("Operator Fusion" guide, section 3: softmax
+ * + cross-entropy is fusible).  Level 1 is the running row max, level 2 the
+ * running sum of exp(z - max), rescaled whenever the max rises (RedFuser's
+ * incremental form); loss = max + ln(sum) - z[target].  Logits are read once.
+ *
+ *   logits  [rows, vocab] dtype      (read)
+ *   targets [rows]        int64      (read; class index, or ignore_index)
+ *   loss    [rows]        fp32       (written; 0 for an ignored row, NaN for a
+ *                                     target outside [0, vocab))
+ *   lse     [rows]        fp32, nullable (written: natural-log sum exp)
+ *   grad    [rows, vocab] dtype, nullable (written: softmax(z) - onehot(target),
+ *                                     unscaled; all zero for an ignored row)
+ *
+ * Supported: dtype RF_F32 / RF_F16 / RF_BF16; vocab a multiple of 16 bytes'
+ * worth of elements (8 for 16-bit, 4 for fp32); logits and grad 16-byte
+ * aligned.  One CTA per row: sized for rows in the thousands (training
+ * batches); any rows >= 1 is correct.
+ * Errors: RF_ERR_INVALID_ARG for null logits/targets/loss, non-positive sizes,
+ * misalignment or a vocab that is not a whole number of vectors; RF_ERR_CUDA
+ * if the launch fails.
+ */
+rf_status_t rf_softmax_xent(const void* logits, const long long* targets, float* loss, float* lse, void* grad,
+                            int rows, int vocab, long long ignore_index, rf_dtype_t dtype, void* stream);
+
 /* Message for the last non-OK status returned on this host thread ("" if none). */
 const char* rf_last_error(void);
 

@@ -24,6 +24,10 @@ incremental form that the CUDA kernels use:
 * ``layernorm``     -- residual add then mean -> biased variance -> normalise
   and affine ("Operator Fusion" guide, section 2, Pattern 2 "Reduction +
   Element-wise"; section 4 "Manual (CUDA)").
+* ``rmsnorm``       -- residual add then mean of squares -> normalise and scale
+  ("Operator Fusion" guide, section 3, fusible patterns: RMSNorm).
+* ``softmax_xent``  -- row max -> sum exp -> cross-entropy loss, its LSE and
+  gradient ("Operator Fusion" guide, section 3: softmax + cross-entropy).
 
 Every function is pinned by the CPU tests (brute force on tiny inputs, closed
 forms, invariants, a library second opinion); no function is "parity unpinned".
@@ -34,5 +38,7 @@ from .reference import (  # noqa: F401
     decode_partials,
     layernorm,
     lse_merge,
+    rmsnorm,
+    softmax_xent,
     split_bounds,
 )

@@ -167,3 +167,45 @@ def layernorm(x, residual, gamma, beta, eps):
     var = ((h - mean) ** 2).sum(axis=-1, keepdims=True) / n  # pass 2 (biased)
     y = (h - mean) / np.sqrt(var + eps) * g + b            # pass 3
     return y, h
+
+
+def rmsnorm(x, residual, gamma, eps):
+    """Residual add followed by RMSNorm over the last axis.
+
+    "Operator Fusion", section 3, lists RMSNorm beside LayerNorm as a fusible
+    reduction + normalise pattern but prints no formula.  Reading (the usual
+    definition): one reduction level, the mean of squares, then the element-wise
+    level y = h / sqrt(mean(h^2) + eps) * gamma, with eps inside the root as in
+    the guide's LayerNorm kernels and no bias.  Returns (y, h) with h = x + r.
+    """
+    x, r, g = _f64(x), _f64(residual), _f64(gamma)
+    h = x + r
+    n = h.shape[-1]
+    ms = (h * h).sum(axis=-1, keepdims=True) / n          # the one reduction level
+    y = h / np.sqrt(ms + eps) * g                          # element-wise level
+    return y, h
+
+
+def softmax_xent(logits, targets, ignore_index=-100):
+    """Softmax cross-entropy per row, with its log-sum-exp and gradient.
+
+    "Operator Fusion", section 3, lists softmax + cross-entropy (training loss)
+    as a fusible pattern; it is a cascade of the same kind as attention's
+    softmax: the row maximum m (level 1, reduce op max), l = sum_j exp(z_j - m)
+    (level 2, reduce op +), then loss = m + ln l - z_target.  Readings: natural
+    log; a row whose target equals ``ignore_index`` has loss 0 and gradient 0;
+    the gradient is d loss / d z = softmax(z) - onehot(target), unscaled.
+    Returns (loss [rows], lse [rows], grad [rows, V]) as float64.
+    """
+    z = _f64(logits)
+    t = np.asarray(targets.detach().cpu().numpy() if hasattr(targets, "detach") else targets, dtype=np.int64)
+    m = z.max(axis=-1, keepdims=True)                     # level 1
+    l = np.exp(z - m).sum(axis=-1, keepdims=True)         # level 2
+    lse = (m + np.log(l))[..., 0]
+    valid = t != ignore_index
+    tz = np.where(valid, z[np.arange(z.shape[0]), np.where(valid, t, 0)], 0.0)
+    loss = np.where(valid, lse - tz, 0.0)
+    grad = np.exp(z - lse[:, None])
+    grad[np.arange(z.shape[0])[valid], t[valid]] -= 1.0
+    grad[~valid] = 0.0
+    return loss, lse, grad

@@ -27,6 +27,12 @@ MUTANTS = {
     "ln_eps_outside_sqrt": ("np.sqrt(var + eps)", "(np.sqrt(var) + eps)"),
     "ln_residual_dropped": ("h = x + r ", "h = x + 0 * r "),
     "ln_beta_scaled": ("* g + b ", "* (g + b) "),
+    "rms_mean_not_squared": ("ms = (h * h).sum(", "ms = (h * np.abs(h) * 0 + h).sum("),
+    "rms_eps_outside_sqrt": ("np.sqrt(ms + eps) * g", "(np.sqrt(ms) + eps) * g"),
+    "xent_target_sign": ("loss = np.where(valid, lse - tz, 0.0)", "loss = np.where(valid, lse + tz, 0.0)"),
+    "xent_lse_missing_max": ("lse = (m + np.log(l))[..., 0]", "lse = (np.log(l))[..., 0]"),
+    "xent_grad_no_onehot": ("t[valid]] -= 1.0", "t[valid]] -= 0.0"),
+    "rms_residual_dropped": ("    h = x + r\n    n = h.shape[-1]\n    ms", "    h = x + 0 * r\n    n = h.shape[-1]\n    ms"),
 }
 
 
@@ -40,5 +46,5 @@ def apply(name):
         raise RuntimeError(f"mutant {name}: snippet found {src.count(old)} times")
     code = compile(src.replace(old, new), ref.__file__, "exec")
     exec(code, ref.__dict__)
-    for fn in ("attention", "decode", "decode_partials", "layernorm", "lse_merge", "split_bounds"):
+    for fn in ("attention", "decode", "decode_partials", "layernorm", "lse_merge", "split_bounds", "rmsnorm", "softmax_xent"):
         setattr(oracle, fn, getattr(ref, fn))

@@ -132,3 +132,31 @@ def test_binding_refuses_cpu_tensors(lib):
     x = torch.zeros(4, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA tensor"):
         rf.rf_layernorm_fused(x, x, None, None, x)
+
+
+@pytest.mark.parametrize("args,status,msg", [
+    ((None, P, P, P, None, 4, 64, 1e-5, 2), rf.RF_ERR_INVALID_ARG, "non-null"),
+    ((P, P, P, None, None, 4, 64, 1e-5, 2), rf.RF_ERR_INVALID_ARG, "non-null"),
+    ((P, P, P, P, None, 4, 0, 1e-5, 2), rf.RF_ERR_INVALID_ARG, "positive"),
+    ((P, P, P, P, None, 4, 64, float("inf"), 2), rf.RF_ERR_INVALID_ARG, "eps"),
+    ((P, MIS, P, P, None, 4, 64, 1e-5, 2), rf.RF_ERR_INVALID_ARG, "aligned"),
+    ((P, P, P, P, None, 4, 20, 1e-5, 1), rf.RF_ERR_INVALID_ARG, "multiple of 8"),
+    ((P, P, P, P, None, 4, 40000, 1e-5, 2), rf.RF_ERR_UNSUPPORTED, "exceeds"),
+])
+def test_rmsnorm_rejects(lib, args, status, msg):
+    assert lib.rf_rmsnorm_fused(*args, S) == status
+    assert msg in lib.rf_last_error().decode()
+
+
+@pytest.mark.parametrize("args,status,msg", [
+    ((None, P, P, None, None, 4, 64, -100, 2), rf.RF_ERR_INVALID_ARG, "non-null"),
+    ((P, None, P, None, None, 4, 64, -100, 2), rf.RF_ERR_INVALID_ARG, "non-null"),
+    ((P, P, P, None, None, 0, 64, -100, 2), rf.RF_ERR_INVALID_ARG, "positive"),
+    ((P, P, P, None, MIS, 4, 64, -100, 2), rf.RF_ERR_INVALID_ARG, "aligned"),
+    ((P, P, P, None, None, 4, 100, -100, 2), rf.RF_ERR_INVALID_ARG, "multiple of 8"),
+    ((P, P, P, None, None, 4, 102, -100, 0), rf.RF_ERR_INVALID_ARG, "multiple of 4"),
+    ((P, P, P, None, None, 4, 64, -100, 5), rf.RF_ERR_INVALID_ARG, "dtype"),
+])
+def test_softmax_xent_rejects(lib, args, status, msg):
+    assert lib.rf_softmax_xent(*args, S) == status
+    assert msg in lib.rf_last_error().decode()

@@ -102,3 +102,37 @@ def test_layernorm_full_size_sampled(rf):
     ref, _ = oracle.layernorm(x[rows], r[rows], g, b, w.dims["eps"])
     check16(y[rows], ref, "full-size sampled rows")
     assert torch.isfinite(y.float()).all()
+
+
+# ---------------------------------------------------------------- RMSNorm
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("rows,cols", [(1, 8), (7, 520), (33, 1024), (4, 4096), (3, 4104), (2, 16384)])
+def test_rmsnorm_shapes(rf, dtype, rows, cols):
+    x, r, g, _ = inputs.ln_inputs(rows, cols, dtype, seed=rows + 3 * cols)
+    y = rf.rmsnorm(x.cuda(), r.cuda(), g.cuda(), eps=1e-5)
+    torch.cuda.synchronize()
+    ref, _ = oracle.rmsnorm(x, r, g, 1e-5)
+    check(dtype, y, ref, f"rms {dtype} {rows}x{cols}")
+
+
+def test_rmsnorm_optional_operands_and_residual_out(rf):
+    x, r, g, _ = inputs.ln_inputs(5, 2048, "bf16", seed=31)
+    y = rf.rmsnorm(x.cuda(), None, None, eps=1e-6)
+    torch.cuda.synchronize()
+    ref, _ = oracle.rmsnorm(x, torch.zeros_like(x), torch.ones_like(g), 1e-6)
+    check16(y, ref, "rms plain")
+    y, h = rf.rmsnorm(x.cuda(), r.cuda(), g.cuda(), eps=1e-5, want_residual_out=True)
+    torch.cuda.synchronize()
+    ref, href = oracle.rmsnorm(x, r, g, 1e-5)
+    check16(y, ref, "rms with residual_out")
+    np.testing.assert_array_equal(to64(h), torch.from_numpy(href).float().to(torch.bfloat16).float().numpy())
+
+
+@pytest.mark.slow
+def test_rmsnorm_full_size_sampled(rf):
+    w = inputs.WORKLOADS["rmsnorm_residual_bf16"]
+    x, r, g = inputs.make(w)
+    y = rf.rmsnorm(x.cuda(), r.cuda(), g.cuda(), eps=w.dims["eps"]).cpu()
+    rows = np.unique(np.concatenate([[0, w.dims["rows"] - 1], np.random.default_rng(2).integers(0, w.dims["rows"], 126)]))
+    ref, _ = oracle.rmsnorm(x[rows], r[rows], g, w.dims["eps"])
+    check16(y[rows], ref, "rms full-size sampled rows")

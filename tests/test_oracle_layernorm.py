@@ -126,3 +126,55 @@ def test_welford_chan_incremental_form_reaches_plain_result():
     n, mean, m2 = tot
     yy = (h[0] - mean) / math.sqrt(m2 / n + 1e-5)
     np.testing.assert_allclose(yy, y[0], atol=1e-12)
+
+
+# ---------------------------------------------------------------- RMSNorm
+def brute_rms(x, r, g, eps):
+    y = np.zeros_like(x)
+    for i in range(x.shape[0]):
+        h = [x[i, j] + r[i, j] for j in range(x.shape[1])]
+        ms = math.fsum(t * t for t in h) / len(h)
+        for j in range(len(h)):
+            y[i, j] = h[j] / math.sqrt(ms + eps) * g[j]
+    return y
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 1), (3, 7), (2, 33)])
+def test_rms_brute_force(rows, cols):
+    x, r, g = _rand((rows, cols), 21), _rand((rows, cols), 22), _rand((cols,), 23)
+    y, h = oracle.rmsnorm(x, r, g, 1e-5)
+    np.testing.assert_allclose(y, brute_rms(x, r, g, 1e-5), atol=1e-12)
+    np.testing.assert_array_equal(h, x + r)
+
+
+def test_rms_unit_mean_square_and_closed_form():
+    x = _rand((6, 40), 24) * 3
+    y, _ = oracle.rmsnorm(x, np.zeros_like(x), np.ones(40), 0.0)
+    np.testing.assert_allclose((y ** 2).mean(-1), 1.0, atol=1e-12)
+    # a constant row c gives c / sqrt(c^2 + eps) * gamma
+    c, eps = -1.75, 1e-3
+    g = _rand((9,), 25)
+    y, _ = oracle.rmsnorm(np.full((1, 9), c), np.zeros((1, 9)), g, eps)
+    np.testing.assert_allclose(y[0], c / math.sqrt(c * c + eps) * g, atol=1e-12)
+
+
+def test_rms_scale_invariance_without_eps():
+    x = _rand((3, 16), 26)
+    g = _rand((16,), 27)
+    y1, _ = oracle.rmsnorm(x, np.zeros_like(x), g, 0.0)
+    y2, _ = oracle.rmsnorm(7.5 * x, np.zeros_like(x), g, 0.0)
+    np.testing.assert_allclose(y1, y2, atol=1e-12)
+    # unlike LayerNorm, a constant shift changes the result
+    y3, _ = oracle.rmsnorm(x + 3.0, np.zeros_like(x), g, 0.0)
+    assert np.abs(y3 - y1).max() > 0.1
+
+
+def test_rms_torch_second_opinion():
+    x = torch.randn(4, 64, dtype=torch.float64, generator=torch.Generator().manual_seed(5))
+    r = torch.randn(4, 64, dtype=torch.float64, generator=torch.Generator().manual_seed(6))
+    g = torch.rand(64, dtype=torch.float64, generator=torch.Generator().manual_seed(7)) + 0.5
+    if not hasattr(torch.nn.functional, "rms_norm"):
+        pytest.skip("torch without rms_norm")
+    ref = torch.nn.functional.rms_norm(x + r, (64,), g, eps=1e-5)
+    y, _ = oracle.rmsnorm(x.numpy(), r.numpy(), g.numpy(), 1e-5)
+    np.testing.assert_allclose(y, ref.numpy(), atol=1e-12)
