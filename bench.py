@@ -138,7 +138,11 @@ class Runner:
         self.dtype = self.w.dtype
         if self.w.kind == "attn":
             self.scale = float(np.float32(1.0 / math.sqrt(d["D"])))
-            self.flops = workmodel.attn_flops(d["B"], d["Hq"], d["N"], d["N"], d["D"], d["causal"])
+            self.flops = workmodel.attn_flops(d["B"], d["Hq"], d["N"], d["N"], d["D"], d["causal"], d.get("window", 0))
+            self.window = d.get("window", 0)
+            self.alibi = None
+            if d.get("alibi"):
+                self.alibi = rf.alibi_slopes(d["Hq"], device=dev)
             self.bytes = workmodel.attn_bytes(d["B"], d["Hq"], d["Hkv"], d["N"], d["N"], d["D"], self.dtype)
             self.metric, self.unit, self.bound = "attention forward TFLOP/s", "TFLOP/s", "tensor"
             self.units = self.flops / 1e12
@@ -198,7 +202,10 @@ class Runner:
     def step(self, ins=None):
         rf, d = self.rf, self.w.dims
         ins = ins or self.dev_in
-        if self.w.kind == "attn":
+        if self.w.kind == "attn" and (self.window or self.alibi is not None):
+            rf.rf_attn_fwd_ex(ins[0], ins[1], ins[2], self.o, self.lse, scale=self.scale, causal=bool(d["causal"]),
+                              window=self.window, alibi_slopes=self.alibi)
+        elif self.w.kind == "attn":
             rf.rf_attn_fwd(ins[0], ins[1], ins[2], self.o, self.lse, scale=self.scale, causal=bool(d["causal"]))
         elif self.w.kind == "decode":
             rf.rf_attn_decode_splitkv(ins[0], ins[1], ins[2], self.o, self.ws, d["splits"], lse=self.lse,

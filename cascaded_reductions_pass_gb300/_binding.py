@@ -30,8 +30,14 @@ DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 _lib = None
 
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+
+
+class AttnOpts(ctypes.Structure):
+    """rf_attn_opts_t: causal mask, sliding window, ALiBi slopes (device fp32 [Hq])."""
+    _fields_ = [("causal", ctypes.c_int), ("window", ctypes.c_int), ("alibi_slopes", ctypes.c_void_p)]
 _SIGNATURES = {
     "rf_attn_fwd": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp], _i),
+    "rf_attn_fwd_ex": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, ctypes.POINTER(AttnOpts), _i, _vp], _i),
     "rf_attn_decode_splitkv_workspace_bytes": ([_i, _i, _i, _i], _sz),
     "rf_attn_decode_splitkv": ([_vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _i, _f, _i, _vp], _i),
     "rf_attn_decode_splitkv_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp], _i),
@@ -138,6 +144,25 @@ def rf_attn_fwd(q, k, v, o, lse=None, scale=None, causal=False, stream=None):
                               B, Hq, Hkv, Nq, Nk, D, scale, int(bool(causal)), _code(q.dtype), _stream(stream)))
 
 
+def rf_attn_fwd_ex(q, k, v, o, lse=None, scale=None, causal=False, window=0, alibi_slopes=None, stream=None):
+    """rf_attn_fwd with a sliding window (key j visible iff i - window < j <= i) and/or
+    ALiBi slopes (float32 CUDA tensor [Hq]); both need causal=True."""
+    B, Hq, Nq, D = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, Hkv, Nk, D) or tuple(v.shape) != tuple(k.shape) or tuple(o.shape) != tuple(q.shape):
+        raise ValueError("shape mismatch among q, k, v, o")
+    if not (q.dtype == k.dtype == v.dtype == o.dtype):
+        raise ValueError("q, k, v and o must share a dtype")
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, Nq)):
+        raise ValueError("lse must be float32 [B,Hq,Nq]")
+    if alibi_slopes is not None and (alibi_slopes.dtype != torch.float32 or alibi_slopes.numel() != Hq):
+        raise ValueError("alibi_slopes must be float32 with Hq elements")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    opts = AttnOpts(int(bool(causal)), int(window), _dev(alibi_slopes, "alibi_slopes", True))
+    _check(load().rf_attn_fwd_ex(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(o, "o"), _dev(lse, "lse", True),
+                                 B, Hq, Hkv, Nq, Nk, D, scale, ctypes.byref(opts), _code(q.dtype), _stream(stream)))
+
+
 def rf_attn_decode_splitkv_workspace_bytes(B, Hq, D, num_splits) -> int:
     return load().rf_attn_decode_splitkv_workspace_bytes(B, Hq, D, num_splits)
 
@@ -239,12 +264,22 @@ def rf_softmax_xent(logits, targets, loss, lse=None, grad=None, ignore_index=-10
                                   _code(logits.dtype), _stream(stream)))
 
 
+def alibi_slopes(n_heads, device="cuda"):
+    """ALiBi head slopes, the geometric sequence 2^(-8 (h+1) / H), as float32 [H]."""
+    return torch.tensor([2.0 ** (-8.0 * (h + 1) / n_heads) for h in range(n_heads)], dtype=torch.float32,
+                        device=device)
+
+
 # ------------------------------------------------------------------ allocating helpers
-def attention(q, k, v, scale=None, causal=False, stream=None):
-    """Allocate (o, lse) and run rf_attn_fwd."""
+def attention(q, k, v, scale=None, causal=False, window=0, alibi_slopes=None, stream=None):
+    """Allocate (o, lse) and run rf_attn_fwd (rf_attn_fwd_ex for a window or ALiBi)."""
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
-    rf_attn_fwd(q, k, v, o, lse, scale=scale, causal=causal, stream=stream)
+    if window or alibi_slopes is not None:
+        rf_attn_fwd_ex(q, k, v, o, lse, scale=scale, causal=causal, window=window, alibi_slopes=alibi_slopes,
+                       stream=stream)
+    else:
+        rf_attn_fwd(q, k, v, o, lse, scale=scale, causal=causal, stream=stream)
     return o, lse
 
 
@@ -298,6 +333,7 @@ def layernorm(x, residual, gamma, beta, eps=1e-5, want_residual_out=False, strea
 
 __all__ = [
     "RFError", "load", "declared_symbols", "rf_version", "rf_last_error", "rf_device_status", "rf_attn_fwd",
+    "rf_attn_fwd_ex", "AttnOpts", "alibi_slopes",
     "rf_attn_decode_splitkv_workspace_bytes", "rf_attn_decode_splitkv", "rf_attn_decode_splitkv_noalloc",
     "rf_lse_merge", "rf_layernorm_fused", "rf_rmsnorm_fused", "rmsnorm", "rf_softmax_xent", "softmax_xent",
     "attention", "decode", "decode_workspace", "decode_partials_view", "layernorm",

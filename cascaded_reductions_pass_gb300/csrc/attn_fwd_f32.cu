@@ -11,7 +11,10 @@
 // this path uses FFMA throughout with the accurate expf/logf.
 //
 // CTA: 4 warps, 16 query rows (4 per warp), key tiles of 32 (one key per
-// lane) staged in shared memory with K rows padded to D+4 floats.
+// lane) staged in shared memory with K rows padded to D+4 floats.  With the
+// causal mask a sliding window (key j visible to query i iff i - window < j)
+// and ALiBi biases (+ slope_h * (j - i)) are supported as in the tensor-core
+// path.
 #include <math.h>
 
 #include "rf_device.cuh"
@@ -29,7 +32,8 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const float* __re
                                                                const float* __restrict__ k,
                                                                const float* __restrict__ v, float* __restrict__ o,
                                                                float* __restrict__ lse, int Hq, int Hkv, int Nq,
-                                                               int Nk, int D, float scale, int causal) {
+                                                               int Nk, int D, float scale, int causal, int window,
+                                                               const float* __restrict__ alibi) {
   extern __shared__ float4 smem4[];
   float* smem = reinterpret_cast<float*>(smem4);
   const int KS = D + 4;               // padded K row stride (floats)
@@ -63,7 +67,10 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const float* __re
 
   const int last_row = min(q0 + kBM, Nq) - 1;
   const int kend = causal ? min(Nk, last_row + 1) : Nk;  // keys past the CTA's last row are all masked
-  for (int k0 = 0; k0 < kend; k0 += kBN) {
+  // a sliding window hides every key below the first row's window
+  const int kbeg = (causal && window > 0) ? (max(0, q0 - window + 1) / kBN) * kBN : 0;
+  const float slope = alibi ? __ldg(alibi + h) : 0.f;
+  for (int k0 = kbeg; k0 < kend; k0 += kBN) {
     __syncthreads();
     for (int i = threadIdx.x; i < kBN * D4; i += blockDim.x) {
       const int r = i / D4, c = i - r * D4;
@@ -92,8 +99,8 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const float* __re
         dot = fmaf(a.z, c.z, dot);
         dot = fmaf(a.w, c.w, dot);
       }
-      const bool visible = key < Nk && (!causal || key <= qi);
-      const float s = visible ? dot * scale : -INFINITY;
+      const bool visible = key < Nk && (!causal || key <= qi) && (window <= 0 || key > qi - window);
+      const float s = visible ? fmaf(slope, static_cast<float>(key - qi), dot * scale) : -INFINITY;
       const float m_new = fmaxf(m[r], warp_max(s));
       if (m_new == -INFINITY) continue;  // no visible key for this row yet
       const float alpha = expf(m[r] - m_new);  // 0 when m was -inf
@@ -133,16 +140,17 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const float* __re
 }  // namespace
 
 cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B, int Hq,
-                            int Hkv, int Nq, int Nk, int D, float scale, int causal, cudaStream_t s) {
+                            int Hkv, int Nq, int Nk, int D, float scale, int causal, int window, const float* alibi,
+                            cudaStream_t s) {
   const dim3 grid((Nq + kBM - 1) / kBM, Hq, B);
   if (B > 65535 || Hq > 65535) return cudaErrorInvalidConfiguration;
   const size_t smem = sizeof(float) * (kBM * D + kBN * (D + 4) + kBN * D);
   const int dc = (D + 31) / 32;
   switch (dc) {
-    case 1: attn_f32_kernel<1><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal); break;
-    case 2: attn_f32_kernel<2><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal); break;
-    case 3: attn_f32_kernel<3><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal); break;
-    default: attn_f32_kernel<4><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal); break;
+    case 1: attn_f32_kernel<1><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi); break;
+    case 2: attn_f32_kernel<2><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi); break;
+    case 3: attn_f32_kernel<3><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi); break;
+    default: attn_f32_kernel<4><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi); break;
   }
   return cudaGetLastError();
 }

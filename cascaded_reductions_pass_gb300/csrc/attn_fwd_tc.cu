@@ -85,11 +85,16 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, unsigned parity) {
   return __all_sync(0xffffffffu, ok);
 }
 
-template <Dt DT, int D, bool CAUSAL>
+// MASK: 0 none, 1 causal (top-left), 2 causal with a sliding window of
+// `window` keys (key j visible to query i iff i - window < j <= i).
+// ALIBI: add slope_h * (j - i) to each scaled score (slopes per query head).
+template <Dt DT, int D, int MASK, bool ALIBI>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, uint16_t* __restrict__ o, float* __restrict__ lse,
-                   int Hq, int Hkv, int Nq, int Nk, int BH, int nqt, float sl2, unsigned* status) {
+                   int Hq, int Hkv, int Nq, int Nk, int BH, int nqt, float sl2, int window,
+                   const float* __restrict__ alibi, unsigned* status) {
+  constexpr bool CAUSAL = MASK >= 1;
   using C = Cfg<D>;
   constexpr int S = C::kStages;
   constexpr bool kBF16 = DT == Dt::BF16;
@@ -107,9 +112,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h = bh % Hq, b = bh / Hq;
   const int kv_plane = b * Hkv + h / (Hq / Hkv);
   const int r0 = c * 2 * kBM;
+  // Key tiles [lo_t, nt_t) that query tile t can see; the CTA streams
+  // [lo0, nt1) (tile 1's rows come after tile 0's, so lo0 <= lo1, nt0 <= nt1).
   const int n_kv = (Nk + kBN - 1) / kBN;
   const int nt0 = CAUSAL ? min(r0 / kBN + 1, n_kv) : n_kv;
   const int nt1 = CAUSAL ? min(r0 / kBN + 2, n_kv) : n_kv;
+  const int lo0 = MASK == 2 ? max(0, r0 - window + 1) / kBN : 0;
+  const int lo1 = MASK == 2 ? max(0, r0 + kBM - window + 1) / kBN : 0;
+  const int n_load = nt1 - lo0;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -157,19 +167,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d_elect(sQ + t * C::kQBytes + bx * (kBM * 128), &tq, &bars->q_full, bx * 64, r0 + t * kBM, bh);
       int issued_k = 0, issued_v = 0;
       bool ok = true;
-      for (int j = 0; j < nt1; ++j) {
-        const int st = j % S;
-        if (j >= S && !(ok = mbar_wait_warp(&bars->k_empty[st], ((j / S) - 1) & 1))) break;
+      for (int jj = 0; jj < n_load; ++jj) {  // ring slot jj holds key tile lo0 + jj
+        const int st = jj % S, key0 = (lo0 + jj) * kBN;
+        if (jj >= S && !(ok = mbar_wait_warp(&bars->k_empty[st], ((jj / S) - 1) & 1))) break;
         mbar_expect_tx_elect(&bars->k_full[st], C::kKVBytes);
 #pragma unroll
         for (int bx = 0; bx < D / 64; ++bx)
-          tma_load_3d_elect(sK + st * C::kKVBytes + bx * (kBN * 128), &tk, &bars->k_full[st], bx * 64, j * kBN, kv_plane);
+          tma_load_3d_elect(sK + st * C::kKVBytes + bx * (kBN * 128), &tk, &bars->k_full[st], bx * 64, key0, kv_plane);
         ++issued_k;
-        if (j >= S && !(ok = mbar_wait_warp(&bars->v_empty[st], ((j / S) - 1) & 1))) break;
+        if (jj >= S && !(ok = mbar_wait_warp(&bars->v_empty[st], ((jj / S) - 1) & 1))) break;
         mbar_expect_tx_elect(&bars->v_full[st], C::kKVBytes);
 #pragma unroll
         for (int bx = 0; bx < D / 64; ++bx)
-          tma_load_3d_elect(sV + st * C::kKVBytes + bx * (kBN * 128), &tv, &bars->v_full[st], bx * 64, j * kBN, kv_plane);
+          tma_load_3d_elect(sV + st * C::kKVBytes + bx * (kBN * 128), &tv, &bars->v_full[st], bx * 64, key0, kv_plane);
         ++issued_v;
       }
       if (!ok) {
@@ -212,81 +222,94 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < kBN / 16; ++kk)
           tc_mma_ts_elect(dO, pcol + kk * 8, b0 + kk * (16 * 128 / 16), idPV, (acc || kk > 0) ? 1u : 0u);
       };
+      // Key tile j (ring slot jj = j - lo0) feeds query tile t when lo_t <= j < nt_t;
+      // barrier phases of tile t count its own key tiles (j - lo_t).
+      auto in0 = [&](int j) { return j >= lo0 && j < nt0; };
+      auto in1 = [&](int j) { return j >= lo1 && j < nt1; };
       bool ok = mbar_wait_warp(&bars->q_full, 0) && mbar_wait_warp(&bars->k_full[0], 0);
       if (ok) {
         tc_fence_after();
-        issue_s(0, 0);
-        tc_commit_elect(&bars->s_full[0]);
-        issue_s(1, 0);
-        tc_commit_elect(&bars->s_full[1]);
+        if (in0(lo0)) {
+          issue_s(0, 0);
+          tc_commit_elect(&bars->s_full[0]);
+        }
+        if (in1(lo0)) {
+          issue_s(1, 0);
+          tc_commit_elect(&bars->s_full[1]);
+        }
         tc_commit_elect(&bars->k_empty[0]);
       }
-      int st = 0, ph = 0;  // ring stage and phase of tile j
-      for (int j = 0; ok && j < nt1; ++j) {
-        const int jn = j + 1;
+      int st = 0, ph = 0;  // ring stage and phase of key tile j
+      for (int jj = 0; ok && jj < n_load; ++jj) {
+        const int j = lo0 + jj, jn = j + 1;
         const int stn = st + 1 == S ? 0 : st + 1, phn = st + 1 == S ? ph ^ 1 : ph;  // stage / phase of j+1
         bool k_ready = false;
         if constexpr (C::kSepP) {
           // S_t(j+1) as soon as softmax t has read S_t(j); PV_t(j) once P_t(j) is ready.
-          if (jn < nt0) {
-            if (!(ok = mbar_wait_warp(&bars->s_free[0], j & 1) && mbar_wait_warp(&bars->k_full[stn], phn))) break;
-            k_ready = true;
-            tc_fence_after();
-            issue_s(0, stn);
-            tc_commit_elect(&bars->s_full[0]);
-          }
-          if (!(ok = mbar_wait_warp(&bars->v_full[st], ph))) break;
-          if (j < nt0) {
-            if (!(ok = mbar_wait_warp(&bars->p_ready[0], j & 1))) break;
-            tc_fence_after();
-            issue_pv(0, st, j > 0);
-            tc_commit_elect(&bars->pv_done[0]);
-            if (j == nt0 - 1) tc_commit_elect(&bars->o_final[0]);
-          }
-          if (jn < nt1) {
-            if (!(ok = mbar_wait_warp(&bars->s_free[1], j & 1))) break;
-            if (!k_ready && !(ok = mbar_wait_warp(&bars->k_full[stn], phn))) break;
-            tc_fence_after();
-            issue_s(1, stn);
-            tc_commit_elect(&bars->s_full[1]);
-            tc_commit_elect(&bars->k_empty[stn]);
-          }
-          if (!(ok = mbar_wait_warp(&bars->p_ready[1], j & 1))) break;
-          tc_fence_after();
-          issue_pv(1, st, j > 0);
-          tc_commit_elect(&bars->pv_done[1]);
-          tc_commit_elect(&bars->v_empty[st]);
-          if (j == nt1 - 1) tc_commit_elect(&bars->o_final[1]);
-        } else {
-          // P aliases S: PV_t(j) must be issued before S_t(j+1) overwrites it.
-          if (!(ok = mbar_wait_warp(&bars->v_full[st], ph))) break;
-          if (j < nt0) {
-            if (!(ok = mbar_wait_warp(&bars->p_ready[0], j & 1))) break;
-            tc_fence_after();
-            issue_pv(0, st, j > 0);
-            if (j == nt0 - 1) tc_commit_elect(&bars->o_final[0]);
-          }
-          if (jn < nt0) {
+          if (in0(jn)) {
+            if (jn > lo0 && !(ok = mbar_wait_warp(&bars->s_free[0], (jn - 1 - lo0) & 1))) break;
             if (!(ok = mbar_wait_warp(&bars->k_full[stn], phn))) break;
             k_ready = true;
             tc_fence_after();
             issue_s(0, stn);
             tc_commit_elect(&bars->s_full[0]);
           }
-          if (!(ok = mbar_wait_warp(&bars->p_ready[1], j & 1))) break;
-          tc_fence_after();
-          issue_pv(1, st, j > 0);
-          if (j == nt1 - 1) tc_commit_elect(&bars->o_final[1]);
+          if (!(ok = mbar_wait_warp(&bars->v_full[st], ph))) break;
+          if (in0(j)) {
+            if (!(ok = mbar_wait_warp(&bars->p_ready[0], (j - lo0) & 1))) break;
+            tc_fence_after();
+            issue_pv(0, st, j > lo0);
+            tc_commit_elect(&bars->pv_done[0]);
+            if (j == nt0 - 1) tc_commit_elect(&bars->o_final[0]);
+          }
+          if (in1(jn)) {
+            if (jn > lo1 && !(ok = mbar_wait_warp(&bars->s_free[1], (jn - 1 - lo1) & 1))) break;
+            if (!k_ready && !(ok = mbar_wait_warp(&bars->k_full[stn], phn))) break;
+            tc_fence_after();
+            issue_s(1, stn);
+            tc_commit_elect(&bars->s_full[1]);
+          }
+          if (jn < nt1) tc_commit_elect(&bars->k_empty[stn]);
+          if (in1(j)) {
+            if (!(ok = mbar_wait_warp(&bars->p_ready[1], (j - lo1) & 1))) break;
+            tc_fence_after();
+            issue_pv(1, st, j > lo1);
+            tc_commit_elect(&bars->pv_done[1]);
+            if (j == nt1 - 1) tc_commit_elect(&bars->o_final[1]);
+          }
           tc_commit_elect(&bars->v_empty[st]);
-          if (jn < nt1) {
+        } else {
+          // P aliases S: PV_t(j) must be issued before S_t(j+1) overwrites it.
+          if (!(ok = mbar_wait_warp(&bars->v_full[st], ph))) break;
+          if (in0(j)) {
+            if (!(ok = mbar_wait_warp(&bars->p_ready[0], (j - lo0) & 1))) break;
+            tc_fence_after();
+            issue_pv(0, st, j > lo0);
+            if (j == nt0 - 1) tc_commit_elect(&bars->o_final[0]);
+          }
+          if (in0(jn)) {
+            if (!(ok = mbar_wait_warp(&bars->k_full[stn], phn))) break;
+            k_ready = true;
+            tc_fence_after();
+            issue_s(0, stn);
+            tc_commit_elect(&bars->s_full[0]);
+          }
+          if (in1(j)) {
+            if (!(ok = mbar_wait_warp(&bars->p_ready[1], (j - lo1) & 1))) break;
+            tc_fence_after();
+            issue_pv(1, st, j > lo1);
+            if (j == nt1 - 1) tc_commit_elect(&bars->o_final[1]);
+          }
+          tc_commit_elect(&bars->v_empty[st]);
+          if (in1(jn)) {
             if (!k_ready) {
               if (!(ok = mbar_wait_warp(&bars->k_full[stn], phn))) break;
               tc_fence_after();
             }
             issue_s(1, stn);
             tc_commit_elect(&bars->s_full[1]);
-            tc_commit_elect(&bars->k_empty[stn]);
           }
+          if (jn < nt1) tc_commit_elect(&bars->k_empty[stn]);
         }
         st = stn;
         ph = phn;
@@ -309,13 +332,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_off + t * kBN;
     const uint32_t tP = tmem + lane_off + (C::kSepP ? C::kPCol + t * (kBN / 2) : t * kBN);
     const uint32_t tO = tmem + lane_off + C::kOCol + t * D;
-    const int n = t == 0 ? nt0 : nt1;
+    const int jlo = t == 0 ? lo0 : lo1, jhi = t == 0 ? nt0 : nt1;
     const int tile_row0 = r0 + t * kBM;
     const uint64_t sl2x2 = f2pack(sl2, sl2);
+    const float slope2 = ALIBI ? __ldg(alibi + (bh % Hq)) * kLog2e : 0.f;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      if (!(ok = warp_wait(&bars->s_full[t], j & 1))) break;
+    for (int j = jlo; j < jhi; ++j) {
+      const int jt = j - jlo;  // this tile's own key-tile count: barrier phases
+      if (!(ok = warp_wait(&bars->s_full[t], jt & 1))) break;
       tc_fence_after();
       uint32_t s[kBN];
 #pragma unroll
@@ -326,11 +351,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bars->s_free[t]);
       }
       const int key0 = j * kBN;
-      if (key0 + kBN > Nk || (CAUSAL && key0 + kBN - 1 > tile_row0)) {
-        const int lim = CAUSAL ? min(Nk, row + 1) : Nk;  // keys [key0, lim) are visible
+      if (key0 + kBN > Nk || (CAUSAL && key0 + kBN - 1 > tile_row0) ||
+          (MASK == 2 && key0 < tile_row0 + kBM - window)) {
+        const int lim = CAUSAL ? min(Nk, row + 1) : Nk;   // keys below lim ...
+        const int first = MASK == 2 ? row - window + 1 : 0;  // ... and from first on are visible
 #pragma unroll
-        for (int i = 0; i < kBN; ++i)
-          if (key0 + i >= lim) s[i] = __float_as_uint(-INFINITY);
+        for (int c = 0; c < kBN; ++c)
+          if (key0 + c >= lim || key0 + c < first) s[c] = __float_as_uint(-INFINITY);
+      }
+      if constexpr (ALIBI) {  // s <- s * scale * log2 e + slope * log2 e * (key - row)
+        const float base = slope2 * static_cast<float>(key0 - row);
+#pragma unroll
+        for (int c = 0; c < kBN; ++c)
+          s[c] = __float_as_uint(fmaf(__uint_as_float(s[c]), sl2, fmaf(slope2, static_cast<float>(c), base)));
       }
       // level 1: tile max over the row, four independent 3-input max chains
       float mx4[4];
@@ -343,20 +376,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         mx4[q4] = fmaxf(m, __uint_as_float(sq[31]));
       }
       const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      const float mt = mx * sl2;
+      const float mt = ALIBI ? mx : mx * sl2;
       const bool need = mt > m_run + kRescaleThreshold;
       const float m_new = need ? mt : m_run;
-      const float alpha = ex2_ftz(m_run - m_new);
+      // a row can see no key of this tile (sliding window): keep it at zero weight
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = ex2_ftz(m_run - m_use);
       // level 2: P = 2^(s*sl2 - m) (16-bit, packed in registers), running sum in
       // four packed accumulators; all exponentials run before any wait below
-      const uint64_t negm2 = f2pack(-m_new, -m_new);
+      const uint64_t negm2 = f2pack(-m_use, -m_use);
       uint64_t sum2[4];
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) sum2[q4] = f2pack(0.f, 0.f);
       uint32_t pk[kBN / 2];
 #pragma unroll
       for (int e = 0; e < kBN / 2; ++e) {
-        const uint64_t x = fma_f32x2(u2pack(s[2 * e], s[2 * e + 1]), sl2x2, negm2);
+        const uint64_t x = ALIBI ? add_f32x2(u2pack(s[2 * e], s[2 * e + 1]), negm2)
+                                 : fma_f32x2(u2pack(s[2 * e], s[2 * e + 1]), sl2x2, negm2);
         float x0, x1;
         f2unpack(x, x0, x1);
         const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
@@ -364,8 +400,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         pk[e] = Pack<DT>::pack2(p0, p1);
       }
       if constexpr (C::kSepP) {  // PV_t(j-1) must be done before P_t and O_t are touched
-        if (j > 0) {
-          if (!(ok = warp_wait(&bars->pv_done[t], (j - 1) & 1))) break;
+        if (jt > 0) {
+          if (!(ok = warp_wait(&bars->pv_done[t], (jt - 1) & 1))) break;
           tc_fence_after();
         }
       }
@@ -376,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       f2unpack(sumv, sum_lo, sum_hi);
       l_run = fmaf(l_run, alpha, sum_lo + sum_hi);
       // level 3 correction: rescale O in TMEM when some row's max moved
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
+      if (jt > 0 && __any_sync(0xffffffffu, need)) {
         const uint64_t a2 = f2pack(alpha, alpha);
 #pragma unroll
         for (int i = 0; i < D / 32; ++i) {
@@ -433,9 +469,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <Dt DT, int D, bool CAUSAL>
+template <Dt DT, int D, int MASK, bool ALIBI>
 cudaError_t launch_cfg(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-                       int Nq, int Nk, float scale, unsigned* status, cudaStream_t s) {
+                       int Nq, int Nk, float scale, int window, const float* alibi, unsigned* status,
+                       cudaStream_t s) {
   alignas(64) CUtensorMap tq, tk, tv;
   cudaError_t err = cudaSuccess;
   if (!encode_tma_3d_16bit(&tq, q, D, Nq, uint64_t(B) * Hq, kBM, &err)) return err;
@@ -445,31 +482,40 @@ cudaError_t launch_cfg(const void* q, const void* k, const void* v, void* o, flo
   const long long grid = static_cast<long long>(nqt) * B * Hq;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const int smem = Cfg<D>::kTiles + 1024 + static_cast<int>(sizeof(TcBars)) + 64;
-  auto kern = attn_tc_kernel<DT, D, CAUSAL>;
+  auto kern = attn_tc_kernel<DT, D, MASK, ALIBI>;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   kern<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(tq, tk, tv, static_cast<uint16_t*>(o), lse, Hq, Hkv, Nq,
-                                                           Nk, B * Hq, nqt, scale * kLog2e, status);
+                                                           Nk, B * Hq, nqt, scale * kLog2e, window, alibi, status);
   return cudaGetLastError();
 }
 
 template <Dt DT, int D>
 cudaError_t launch_d(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-                     int Nq, int Nk, float scale, int causal, unsigned* status, cudaStream_t s) {
-  return causal ? launch_cfg<DT, D, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, status, s)
-                : launch_cfg<DT, D, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, status, s);
+                     int Nq, int Nk, float scale, int causal, int window, const float* alibi, unsigned* status,
+                     cudaStream_t s) {
+  if (!causal) return launch_cfg<DT, D, 0, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, 0, nullptr, status, s);
+  if (window > 0) {
+    return alibi ? launch_cfg<DT, D, 2, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, window, alibi, status, s)
+                 : launch_cfg<DT, D, 2, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, window, nullptr, status, s);
+  }
+  return alibi ? launch_cfg<DT, D, 1, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, 0, alibi, status, s)
+               : launch_cfg<DT, D, 1, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, 0, nullptr, status, s);
 }
 
 }  // namespace
 
 cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-                           int Nq, int Nk, int D, float scale, int causal, Dt dt, unsigned* status, cudaStream_t s) {
+                           int Nq, int Nk, int D, float scale, int causal, int window, const float* alibi, Dt dt,
+                           unsigned* status, cudaStream_t s) {
   if (dt == Dt::BF16)
-    return D == 128 ? launch_d<Dt::BF16, 128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, status, s)
-                    : launch_d<Dt::BF16, 64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, status, s);
+    return D == 128
+               ? launch_d<Dt::BF16, 128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, alibi, status, s)
+               : launch_d<Dt::BF16, 64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, alibi, status, s);
   if (dt == Dt::F16)
-    return D == 128 ? launch_d<Dt::F16, 128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, status, s)
-                    : launch_d<Dt::F16, 64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, status, s);
+    return D == 128
+               ? launch_d<Dt::F16, 128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, alibi, status, s)
+               : launch_d<Dt::F16, 64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, alibi, status, s);
   return cudaErrorNotSupported;
 }
 

@@ -169,43 +169,73 @@ rf_status_t rf_device_status(void* stream, int clear) {
   return RF_OK;
 }
 
-rf_status_t rf_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                        int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal,
-                        rf_dtype_t dtype, void* stream) {
-  if (!q || !k || !v || !o) return fail(RF_ERR_INVALID_ARG, "rf_attn_fwd: q, k, v and o must be non-null");
+}  // extern "C"
+
+namespace {
+
+rf_status_t attn_impl(const char* name, const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal, int window,
+                      const float* alibi, rf_dtype_t dtype, void* stream) {
+  if (!q || !k || !v || !o) return fail(RF_ERR_INVALID_ARG, "%s: q, k, v and o must be non-null", name);
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || D <= 0)
-    return fail(RF_ERR_INVALID_ARG, "rf_attn_fwd: sizes must be positive (B=%d Hq=%d Hkv=%d Nq=%d Nk=%d D=%d)",
-                B, Hq, Hkv, Nq, Nk, D);
-  if (Hq % Hkv != 0) return fail(RF_ERR_INVALID_ARG, "rf_attn_fwd: Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
+    return fail(RF_ERR_INVALID_ARG, "%s: sizes must be positive (B=%d Hq=%d Hkv=%d Nq=%d Nk=%d D=%d)", name, B, Hq,
+                Hkv, Nq, Nk, D);
+  if (Hq % Hkv != 0) return fail(RF_ERR_INVALID_ARG, "%s: Hq=%d is not a multiple of Hkv=%d", name, Hq, Hkv);
   if (!(scale > 0.0f) || !std::isfinite(scale))
-    return fail(RF_ERR_INVALID_ARG, "rf_attn_fwd: scale must be finite and positive");
-  if (!valid_dtype(dtype)) return fail(RF_ERR_INVALID_ARG, "rf_attn_fwd: unknown dtype %d", int(dtype));
+    return fail(RF_ERR_INVALID_ARG, "%s: scale must be finite and positive", name);
+  if (!valid_dtype(dtype)) return fail(RF_ERR_INVALID_ARG, "%s: unknown dtype %d", name, int(dtype));
+  if (window < 0) return fail(RF_ERR_INVALID_ARG, "%s: window must be >= 0", name);
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
-    return fail(RF_ERR_INVALID_ARG, "rf_attn_fwd: pointers must be 16-byte aligned");
+    return fail(RF_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", name);
+  if ((reinterpret_cast<uintptr_t>(alibi) & 3u) != 0)
+    return fail(RF_ERR_INVALID_ARG, "%s: alibi_slopes must be 4-byte aligned", name);
   if (causal && Nq != Nk)
-    return fail(RF_ERR_UNSUPPORTED, "rf_attn_fwd: causal mask requires Nq == Nk (got %d, %d)", Nq, Nk);
+    return fail(RF_ERR_UNSUPPORTED, "%s: causal mask requires Nq == Nk (got %d, %d)", name, Nq, Nk);
+  if (!causal && (window > 0 || alibi))
+    return fail(RF_ERR_UNSUPPORTED, "%s: a sliding window and ALiBi need the causal mask", name);
   if (dtype == RF_F32) {
     if (D % 4 != 0 || D > 128)
-      return fail(RF_ERR_UNSUPPORTED, "rf_attn_fwd: f32 path needs D %% 4 == 0 and D <= 128 (D=%d)", D);
+      return fail(RF_ERR_UNSUPPORTED, "%s: f32 path needs D %% 4 == 0 and D <= 128 (D=%d)", name, D);
   } else if (D != 64 && D != 128) {
-    return fail(RF_ERR_UNSUPPORTED, "rf_attn_fwd: %s path supports D in {64, 128} (D=%d)", dt_name(dtype), D);
+    return fail(RF_ERR_UNSUPPORTED, "%s: %s path supports D in {64, 128} (D=%d)", name, dt_name(dtype), D);
   }
   RF_TRY(check_dev_ptr(q, "q"));
   RF_TRY(check_dev_ptr(k, "k"));
   RF_TRY(check_dev_ptr(v, "v"));
   RF_TRY(check_dev_ptr(o, "o"));
   RF_TRY(check_dev_ptr(lse, "lse"));
+  RF_TRY(check_dev_ptr(alibi, "alibi_slopes"));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == RF_F32)
     return launched(rf::launch_attn_f32(static_cast<const float*>(q), static_cast<const float*>(k),
-                                        static_cast<const float*>(v), static_cast<float*>(o), lse, B, Hq,
-                                        Hkv, Nq, Nk, D, scale, causal, s),
-                    "rf_attn_fwd(f32)");
+                                        static_cast<const float*>(v), static_cast<float*>(o), lse, B, Hq, Hkv, Nq, Nk,
+                                        D, scale, causal, window, alibi, s),
+                    name);
   unsigned* st = rf::device_status_ptr();
-  if (!st) return fail(RF_ERR_CUDA, "rf_attn_fwd: cannot resolve the device status word");
-  return launched(rf::launch_attn_tc(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal,
+  if (!st) return fail(RF_ERR_CUDA, "%s: cannot resolve the device status word", name);
+  return launched(rf::launch_attn_tc(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi,
                                      static_cast<rf::Dt>(dtype), st, s),
-                  "rf_attn_fwd(tcgen05)");
+                  name);
+}
+
+}  // namespace
+
+extern "C" {
+
+rf_status_t rf_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                        int Nq, int Nk, int D, float scale, int causal, rf_dtype_t dtype, void* stream) {
+  return attn_impl("rf_attn_fwd", q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal ? 1 : 0, 0, nullptr, dtype,
+                   stream);
+}
+
+rf_status_t rf_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                           int Hkv, int Nq, int Nk, int D, float scale, const rf_attn_opts_t* opts,
+                           rf_dtype_t dtype, void* stream) {
+  const int causal = opts ? (opts->causal ? 1 : 0) : 0;
+  const int window = opts ? opts->window : 0;
+  const float* alibi = opts ? opts->alibi_slopes : nullptr;
+  return attn_impl("rf_attn_fwd_ex", q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi, dtype,
+                   stream);
 }
 
 size_t rf_attn_decode_splitkv_workspace_bytes(int B, int Hq, int D, int num_splits) {

@@ -32,7 +32,7 @@ cudaError_t launch_lse_merge(const float* o_part, const float* lse_part, void* o
 // exact fp32 SIMT attention forward (attn_fwd_f32.cu)
 cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, float* o, float* lse,
                             int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal,
-                            cudaStream_t s);
+                            int window, const float* alibi, cudaStream_t s);
 
 // split-KV decode partials (decode_split.cu): writes o_part [B*Hq, S, D] and
 // lse_part [B*Hq, S] fp32.
@@ -43,7 +43,7 @@ cudaError_t launch_decode_split(const void* q, const void* k, const void* v, flo
 // tcgen05 / TMEM / TMA attention forward for 16-bit inputs (attn_fwd_tc.cu)
 cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* o, float* lse,
                            int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal,
-                           Dt dt, unsigned* status, cudaStream_t s);
+                           int window, const float* alibi, Dt dt, unsigned* status, cudaStream_t s);
 
 // TMA descriptor encoding through the driver entry point (rf_api.cu).
 // 3-D tensor [outer][rows][inner] of 16-bit elements, box {64, box_rows, 1},

@@ -121,6 +121,11 @@ WORKLOADS = {
                                       dict(rows=16384, cols=4096, eps=1e-5)),
     "softmax_xent_bf16": Workload("softmax_xent_bf16", "xent", "bf16", 7,
                                   dict(rows=4096, vocab=128256)),
+    # the score variants of AttnFuse's Table 6 on the non-causal workload's shape
+    "attn_sw256_f16_d64": Workload("attn_sw256_f16_d64", "attn", "f16", 8,
+                                   dict(B=4, Hq=12, Hkv=12, N=4096, D=64, causal=1, window=256)),
+    "attn_causal_alibi_f16_d64": Workload("attn_causal_alibi_f16_d64", "attn", "f16", 9,
+                                          dict(B=4, Hq=12, Hkv=12, N=4096, D=64, causal=1, alibi=1)),
 }
 
 

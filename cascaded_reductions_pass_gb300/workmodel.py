@@ -13,7 +13,12 @@ from __future__ import annotations
 ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2}
 
 
-def attn_flops(B, Hq, Nq, Nk, D, causal):
+def attn_flops(B, Hq, Nq, Nk, D, causal, window=0):
+    """A sliding window counts its visible pairs exactly: sum_i min(i + 1, window)."""
+    if causal and window:
+        w = min(window, Nq)
+        pairs = w * (w + 1) / 2.0 + (Nq - w) * window
+        return 4.0 * B * Hq * pairs * D
     full = 4.0 * B * Hq * Nq * Nk * D
     return full / 2.0 if causal else full
 

@@ -84,6 +84,31 @@ rf_status_t rf_attn_fwd(const void* q, const void* k, const void* v, void* o, fl
                         int causal, rf_dtype_t dtype, void* stream);
 
 /*
+ * rf_attn_fwd_ex -- rf_attn_fwd with score variants (AttnFuse, Table 6: a
+ * sliding window W=256 and causal + ALiBi beside dense and causal).
+ *
+ * Options (opts nullable = non-causal, no variant):
+ *   causal        top-left causal mask; requires Nq == Nk.
+ *   window        > 0: a key j is also hidden from query i unless
+ *                 j > i - window (the window counts the query's own key).
+ *                 Key tiles wholly outside every row's window are skipped.
+ *   alibi_slopes  nullable device pointer to Hq fp32 slopes: slope[h]*(j - i)
+ *                 is added to each scaled score (the linear-bias form of ALiBi).
+ * The window and ALiBi need the causal mask (RF_ERR_UNSUPPORTED otherwise).
+ * The LSE output includes the ALiBi bias.  Everything else (layouts,
+ * supported dtypes and head dims, errors) is as rf_attn_fwd; a negative window
+ * is RF_ERR_INVALID_ARG.
+ */
+typedef struct rf_attn_opts_t {
+  int causal;
+  int window;
+  const float* alibi_slopes;
+} rf_attn_opts_t;
+rf_status_t rf_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale,
+                           const rf_attn_opts_t* opts, rf_dtype_t dtype, void* stream);
+
+/*
  * rf_attn_decode_splitkv_workspace_bytes -- scratch size for rf_attn_decode_splitkv:
  * fp32 partial outputs [B*Hq, num_splits, D] followed (at a 256-byte aligned
  * offset) by fp32 partial LSEs [B*Hq, num_splits].  Returns 0 for non-positive

@@ -33,6 +33,7 @@ Every function is pinned by the CPU tests (brute force on tiny inputs, closed
 forms, invariants, a library second opinion); no function is "parity unpinned".
 """
 from .reference import (  # noqa: F401
+    alibi_slopes,
     attention,
     decode,
     decode_partials,

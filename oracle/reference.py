@@ -29,7 +29,7 @@ def _f64(a):
     return np.asarray(a, dtype=np.float64)
 
 
-def attention(q, k, v, scale, causal=False, rows=None):
+def attention(q, k, v, scale, causal=False, rows=None, window=0, alibi_slopes=None):
     """Plain attention forward: O = softmax(scale * Q K^T [+ mask]) V, and LSE.
 
     Follows the unfused listing of "Operator Fusion", section 2, Pattern 4:
@@ -46,7 +46,13 @@ def attention(q, k, v, scale, causal=False, rows=None):
 
     ``rows`` optionally restricts the computation to a list of query indices
     (used for sampled checks at full size); outputs then have len(rows) rows.
-    Returns (o [B,Hq,R,Dv], lse [B,Hq,R]) as float64.
+
+    Score variants (AttnFuse, Table 6: sliding window W=256, causal + ALiBi),
+    both on top of the causal mask.  Readings: ``window`` = W > 0 keeps key j
+    for query i iff i - W < j <= i (the window counts the query's own key);
+    ``alibi_slopes`` [Hq] adds slope_h * (j - i) to each score after the
+    scaling (the linear-bias definition of ALiBi, a non-positive bias for
+    visible keys).  Returns (o [B,Hq,R,Dv], lse [B,Hq,R]) as float64.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Hq, Nq, _ = q.shape
@@ -64,9 +70,13 @@ def attention(q, k, v, scale, causal=False, rows=None):
             kvh = h // group
             # pass 0: the score matrix, materialised in full
             s = (q[b, h, sel, :] @ k[b, kvh].T) * scale
+            key_idx = np.arange(Nk)[None, :]
+            if alibi_slopes is not None:
+                s = s + float(_f64(alibi_slopes)[h]) * (key_idx - sel[:, None])
             if causal:
-                key_idx = np.arange(Nk)[None, :]
                 s = np.where(key_idx <= sel[:, None], s, NEG_INF)
+            if window:
+                s = np.where(key_idx > sel[:, None] - window, s, NEG_INF)
             # level 1: row maximum
             m = s.max(axis=1)
             live = np.isfinite(m)
@@ -209,3 +219,10 @@ def softmax_xent(logits, targets, ignore_index=-100):
     grad[np.arange(z.shape[0])[valid], t[valid]] -= 1.0
     grad[~valid] = 0.0
     return loss, lse, grad
+
+
+def alibi_slopes(n_heads):
+    """Head slopes of ALiBi (the linear-bias definition): the geometric sequence
+    2^(-8 (h+1) / H) for h = 0..H-1.  The pages name ALiBi (AttnFuse, Table 6)
+    without its slopes; this is the usual choice."""
+    return np.array([2.0 ** (-8.0 * (h + 1) / n_heads) for h in range(n_heads)])

@@ -29,6 +29,9 @@ MUTANTS = {
     "ln_beta_scaled": ("* g + b ", "* (g + b) "),
     "rms_mean_not_squared": ("ms = (h * h).sum(", "ms = (h * np.abs(h) * 0 + h).sum("),
     "rms_eps_outside_sqrt": ("np.sqrt(ms + eps) * g", "(np.sqrt(ms) + eps) * g"),
+    "attn_window_off_by_one": ("s = np.where(key_idx > sel[:, None] - window, s, NEG_INF)",
+                               "s = np.where(key_idx >= sel[:, None] - window, s, NEG_INF)"),
+    "attn_alibi_sign": ("* (key_idx - sel[:, None])", "* (sel[:, None] - key_idx)"),
     "xent_target_sign": ("loss = np.where(valid, lse - tz, 0.0)", "loss = np.where(valid, lse + tz, 0.0)"),
     "xent_lse_missing_max": ("lse = (m + np.log(l))[..., 0]", "lse = (np.log(l))[..., 0]"),
     "xent_grad_no_onehot": ("t[valid]] -= 1.0", "t[valid]] -= 0.0"),
@@ -46,5 +49,5 @@ def apply(name):
         raise RuntimeError(f"mutant {name}: snippet found {src.count(old)} times")
     code = compile(src.replace(old, new), ref.__file__, "exec")
     exec(code, ref.__dict__)
-    for fn in ("attention", "decode", "decode_partials", "layernorm", "lse_merge", "split_bounds", "rmsnorm", "softmax_xent"):
+    for fn in ("attention", "decode", "decode_partials", "layernorm", "lse_merge", "split_bounds", "rmsnorm", "softmax_xent", "alibi_slopes"):
         setattr(oracle, fn, getattr(ref, fn))

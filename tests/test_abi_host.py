@@ -160,3 +160,19 @@ def test_rmsnorm_rejects(lib, args, status, msg):
 def test_softmax_xent_rejects(lib, args, status, msg):
     assert lib.rf_softmax_xent(*args, S) == status
     assert msg in lib.rf_last_error().decode()
+
+
+def test_attn_ex_rejects(lib):
+    from cascaded_reductions_pass_gb300._binding import AttnOpts
+
+    def call(opts, **kw):
+        a = dict(B=1, Hq=2, Hkv=1, Nq=8, Nk=8, D=64)
+        a.update(kw)
+        return lib.rf_attn_fwd_ex(P, P, P, P, None, a["B"], a["Hq"], a["Hkv"], a["Nq"], a["Nk"], a["D"], 0.125,
+                                  ctypes.byref(opts) if opts is not None else None, 1, S)
+
+    assert call(AttnOpts(1, -1, None)) == rf.RF_ERR_INVALID_ARG and "window" in lib.rf_last_error().decode()
+    assert call(AttnOpts(0, 16, None)) == rf.RF_ERR_UNSUPPORTED and "causal" in lib.rf_last_error().decode()
+    assert call(AttnOpts(0, 0, 0x10000)) == rf.RF_ERR_UNSUPPORTED
+    assert call(AttnOpts(1, 16, None), Nk=9) == rf.RF_ERR_UNSUPPORTED and "Nq == Nk" in lib.rf_last_error().decode()
+    assert call(AttnOpts(1, 16, 0x10002)) == rf.RF_ERR_INVALID_ARG and "aligned" in lib.rf_last_error().decode()

@@ -102,3 +102,63 @@ def test_full_size_sampled(rf, name):
                                   bool(d["causal"]), rows=rows)
         check16(o[b:b + 1, h:h + 1, rows], ro, f"{name} b={b} h={h}")
         check_lse(lse[b:b + 1, h:h + 1, rows], rl, what=f"{name} lse")
+
+
+# ---------------------------------------------------------------- score variants
+@pytest.mark.parametrize("B,H,N,D,window,alibi,dtype", [
+    (1, 2, 1000, 64, 256, False, "f16"),
+    (1, 2, 700, 128, 256, False, "bf16"),
+    (2, 3, 513, 64, 100, False, "bf16"),    # window below one tile
+    (1, 2, 600, 64, 1, False, "f16"),       # own key only
+    (1, 4, 900, 64, 0, True, "f16"),
+    (1, 2, 640, 128, 0, True, "bf16"),
+    (1, 3, 1100, 64, 300, True, "f16"),     # window and ALiBi together
+    (1, 2, 256, 128, 5000, False, "bf16"),  # window wider than the sequence = causal
+])
+def test_variants(rf, B, H, N, D, window, alibi, dtype):
+    q, k, v = inputs.attn_inputs(B, H, H, N, N, D, dtype, seed=N + window)
+    scale = float(np.float32(1 / np.sqrt(D)))
+    slopes = oracle.alibi_slopes(H) if alibi else None
+    o, lse = rf.attention(q.cuda(), k.cuda(), v.cuda(), scale=scale, causal=True, window=window,
+                          alibi_slopes=torch.tensor(slopes, dtype=torch.float32).cuda() if alibi else None)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention(q, k, v, scale, True, window=window, alibi_slopes=slopes)
+    check16(o.cpu(), ro, f"variant W={window} alibi={alibi}")
+    check_lse(lse.cpu(), rl, what="variant lse")
+
+
+@pytest.mark.parametrize("window,alibi", [(7, False), (0, True), (40, True)])
+def test_variants_f32_path(rf, window, alibi):
+    q, k, v = inputs.attn_inputs(1, 2, 2, 150, 150, 64, "f32", seed=5)
+    slopes = oracle.alibi_slopes(2) if alibi else None
+    o, lse = rf.attention(q.cuda(), k.cuda(), v.cuda(), scale=0.125, causal=True, window=window,
+                          alibi_slopes=torch.tensor(slopes, dtype=torch.float32).cuda() if alibi else None)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention(q, k, v, 0.125, True, window=window, alibi_slopes=slopes)
+    from _parity import check32
+    check32(o.cpu(), ro, "f32 variant")
+    check_lse(lse.cpu(), rl, tol=1e-5 * max(1, np.abs(rl).max()))
+
+
+def test_package_alibi_slopes_match_oracle(rf):
+    np.testing.assert_allclose(rf.alibi_slopes(12, device="cpu").numpy(), oracle.alibi_slopes(12), rtol=1e-7)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["attn_sw256_f16_d64", "attn_causal_alibi_f16_d64"])
+def test_variant_workloads_sampled(rf, name):
+    w = inputs.WORKLOADS[name]
+    d = w.dims
+    q, k, v = inputs.make(w)
+    scale = float(np.float32(1 / np.sqrt(d["D"])))
+    slopes = oracle.alibi_slopes(d["Hq"]) if d.get("alibi") else None
+    o, lse = rf.attention(q.cuda(), k.cuda(), v.cuda(), scale=scale, causal=True, window=d.get("window", 0),
+                          alibi_slopes=torch.tensor(slopes, dtype=torch.float32).cuda() if slopes is not None else None)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([[0, 255, 256, d["N"] - 1], np.random.default_rng(4).integers(0, d["N"], 60)]))
+    for b, h in [(0, 0), (d["B"] - 1, d["Hq"] - 1)]:
+        ro, rl = oracle.attention(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1], scale, True,
+                                  rows=rows, window=d.get("window", 0),
+                                  alibi_slopes=slopes[h:h + 1] if slopes is not None else None)
+        check16(o[b:b + 1, h:h + 1, rows].cpu(), ro, name)
+        check_lse(lse[b:b + 1, h:h + 1, rows].cpu(), rl, what=name)

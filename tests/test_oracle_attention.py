@@ -254,3 +254,54 @@ def test_decode_matches_attention_with_one_query():
     np.testing.assert_allclose(lse, l2[:, :, 0], atol=0)
     o3, l3 = oracle.decode(q[:, :, 0], k, v, 0.25)
     np.testing.assert_allclose(o3, o, atol=0)
+
+
+# ---------------------------------------------------------------- score variants
+def brute_variant(q, k, v, scale, window, slopes):
+    B, Hq, N, D = q.shape
+    o = np.zeros_like(q)
+    lse = np.zeros((B, Hq, N))
+    for h in range(Hq):
+        for i in range(N):
+            keys = [j for j in range(N) if j <= i and (not window or j > i - window)]
+            s = [scale * math.fsum(q[0, h, i, d] * k[0, h, j, d] for d in range(D))
+                 + (slopes[h] * (j - i) if slopes is not None else 0.0) for j in keys]
+            m = max(s)
+            e = [math.exp(x - m) for x in s]
+            t = math.fsum(e)
+            for d in range(D):
+                o[0, h, i, d] = math.fsum(e[a] * v[0, h, keys[a], d] for a in range(len(keys))) / t
+            lse[0, h, i] = m + math.log(t)
+    return o, lse
+
+
+@pytest.mark.parametrize("window,alibi", [(3, False), (1, False), (0, True), (4, True)])
+def test_variants_brute_force(window, alibi):
+    q, k, v = _rand((1, 2, 9, 4), 40), _rand((1, 2, 9, 4), 41), _rand((1, 2, 9, 4), 42)
+    slopes = oracle.alibi_slopes(2) if alibi else None
+    o, lse = oracle.attention(q, k, v, 0.5, True, window=window, alibi_slopes=slopes)
+    ob, lb = brute_variant(q, k, v, 0.5, window, slopes)
+    np.testing.assert_allclose(o, ob, atol=1e-12)
+    np.testing.assert_allclose(lse, lb, atol=1e-12)
+
+
+def test_window_limits():
+    q, k, v = _rand((1, 1, 20, 4), 43), _rand((1, 1, 20, 4), 44), _rand((1, 1, 20, 4), 45)
+    full, lf = oracle.attention(q, k, v, 0.5, True)
+    wide, lw = oracle.attention(q, k, v, 0.5, True, window=20)
+    np.testing.assert_allclose(wide, full, atol=0)
+    np.testing.assert_allclose(lw, lf, atol=0)
+    one, l1 = oracle.attention(q, k, v, 0.5, True, window=1)  # each query sees only its own key
+    np.testing.assert_allclose(one[0, 0], v[0, 0], atol=1e-12)
+    np.testing.assert_allclose(l1[0, 0], 0.5 * (q[0, 0] * k[0, 0]).sum(-1), atol=1e-12)
+
+
+def test_alibi_limits_and_slopes():
+    q, k, v = _rand((1, 2, 12, 4), 46), _rand((1, 2, 12, 4), 47), _rand((1, 2, 12, 4), 48)
+    base, lb = oracle.attention(q, k, v, 0.5, True)
+    zero, lz = oracle.attention(q, k, v, 0.5, True, alibi_slopes=np.zeros(2))
+    np.testing.assert_allclose(zero, base, atol=0)
+    steep, _ = oracle.attention(q, k, v, 0.5, True, alibi_slopes=np.full(2, 500.0))  # bias wins: own key only
+    np.testing.assert_allclose(steep[0, :], v[0, :], atol=1e-12)
+    s = oracle.alibi_slopes(8)
+    np.testing.assert_allclose(s, 2.0 ** (-np.arange(1, 9)), atol=0)
