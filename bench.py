@@ -6,8 +6,10 @@ A step is one call of the hot path on one batch of the workload's synthetic
 input, inputs already resident in HBM.  The default workload is the
 non-causal fp16 attention forward (B=4 H=12 N=4096 D=64, seed 1); the line's
 ``parts`` object reports the other workloads (causal GQA bf16 attention,
-split-KV decode, residual+LayerNorm, tiny fp32 attention) measured the same
-way in the same run.  Each timed step is bracketed by CUDA events on the
+split-KV decode, residual+LayerNorm and RMSNorm, softmax cross-entropy, the
+sliding-window and ALiBi attention variants, tiny fp32 attention) measured the
+same way in the same run, and ``ablations`` times the fusion-level and
+non-incremental variants of the LayerNorm and cross-entropy cascades.  Each timed step is bracketed by CUDA events on the
 launching stream, with an L2 flush (a 512 MiB memset, larger than the 129 MB
 L2) before every step, outside the events.  Under torchrun each rank runs an
 independent replica (no data-path collective: the work of one call does not
@@ -376,6 +378,53 @@ def measure(name, dev, steps, warmup, flush, peaks, with_e2e=True, batch=None):
     return r, res
 
 
+def measure_ablations(dev, steps, warmup, flush, peaks):
+    """Each fusion-level / incremental-form variant of the residual+LayerNorm and
+    softmax cross-entropy workloads (RedFuser, Figures 6-7), timed like a step.
+    ``gbs`` is the fused form's algorithmic bytes over the variant's time, so it
+    compares like for like; ``model_bytes`` is the variant's own compulsory
+    traffic."""
+    import cascaded_reductions_pass_gb300 as rf
+
+    out = {}
+    for name, op, variants in (("layernorm_residual_bf16", "layernorm", rf.LN_VARIANTS),
+                               ("softmax_xent_bf16", "xent", rf.XENT_VARIANTS)):
+        w = inputs.WORKLOADS[name]
+        d = w.dims
+        rows, cols = d["rows"], d["cols" if op == "layernorm" else "vocab"]
+        dev_in = [t.to(dev) for t in inputs.make(w)]
+        if op == "layernorm":
+            o = torch.empty_like(dev_in[0])
+        else:
+            o = torch.empty(rows, dtype=torch.float32, device=dev)
+            lse = torch.empty(rows, dtype=torch.float32, device=dev)
+        fused_bytes = workmodel.ablation_bytes(op, 0, rows, cols, w.dtype)
+        res = {}
+        for v, label in variants.items():
+            ws = rf.ablation_workspace(0 if op == "layernorm" else 1, v, rows, cols, dev_in[0].dtype, dev)
+
+            class _Step:
+                def step(self, _v=v, _ws=ws):
+                    if op == "layernorm":
+                        rf.rf_layernorm_ablation(*dev_in, o, _v, workspace=_ws, eps=d["eps"])
+                    else:
+                        rf.rf_softmax_xent_ablation(dev_in[0], dev_in[1], o, lse, _v, workspace=_ws)
+
+            times = time_steps(_Step(), steps, warmup, flush)
+            ms = float(np.mean(times))
+            res[str(v)] = {"variant": label, "ms": ms, "gbs": fused_bytes / (ms / 1e3) / 1e9,
+                           "model_bytes": workmodel.ablation_bytes(op, v, rows, cols, w.dtype),
+                           "launches": {0: 1, 1: 1, 2: 2, 3: 4}[v] if op == "layernorm" else {0: 1, 1: 1, 2: 3}[v]}
+            del ws
+        base = res["0"]["ms"]
+        for r in res.values():
+            r["slowdown_vs_fused"] = r["ms"] / base
+        out[name] = {"fused_algorithmic_bytes": fused_bytes, "hbm_peak_gbs": peaks["hbm_gbs"], "variants": res}
+        del dev_in
+        torch.cuda.empty_cache()
+    return out
+
+
 def aggregate_over_ranks(local_ms, units_per_rank, world, device=None):
     """Replicas: every rank processed `units_per_rank`; the job's time is the slowest
     rank's.  Returns (max_ms, whole-job value in units/s).  With world > 1 this is a
@@ -478,6 +527,12 @@ def main():
             except Exception as exc:  # a workload whose kernel is unavailable is reported, not hidden
                 parts[name] = {"error": f"{type(exc).__name__}: {exc}"}
             torch.cuda.empty_cache()
+    ablations = None
+    if not args.no_parts and rank == 0:
+        try:
+            ablations = measure_ablations(dev, 10, args.warmup, flush, peaks)
+        except Exception as exc:
+            ablations = {"error": f"{type(exc).__name__}: {exc}"}
     sampler.stop()
     status = rf.rf_device_status()
 
@@ -497,7 +552,7 @@ def main():
             "roofline": res["roofline"],
             "e2e": e2e,
             "gpu_launches": launches, "clocks": clocks, "cpu_baseline": cpu,
-            "device_status": int(status), "parts": parts,
+            "device_status": int(status), "parts": parts, "ablations": ablations,
             "ms_p10": res["ms_p10"], "ms_p90": res["ms_p90"],
         }
         print(json.dumps(line))

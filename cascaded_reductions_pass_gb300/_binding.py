@@ -48,6 +48,10 @@ _SIGNATURES = {
     "rf_last_error": ([], ctypes.c_char_p),
     "rf_version": ([], _i),
     "rf_device_status": ([_vp, _i], _i),
+    "rf_selftest_wait_timeout": ([ctypes.c_uint, _vp], _i),
+    "rf_ablation_workspace_bytes": ([_i, _i, _i, _i, _i], _sz),
+    "rf_layernorm_ablation": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _f, _i, _vp, _sz, _i, _vp], _i),
+    "rf_softmax_xent_ablation": ([_vp, _vp, _vp, _vp, _i, _i, ctypes.c_longlong, _i, _vp, _sz, _i, _vp], _i),
 }
 
 
@@ -127,6 +131,11 @@ def rf_last_error() -> str:
 def rf_device_status(stream=None, clear=True) -> int:
     """Synchronise the stream and return the device status (RF_OK or RF_ERR_TIMEOUT)."""
     return load().rf_device_status(_stream(stream), int(bool(clear)))
+
+
+def rf_selftest_wait_timeout(timeout_us=2000, stream=None):
+    """Launch the bounded-wait self-test (a wait that is meant to run out)."""
+    _check(load().rf_selftest_wait_timeout(int(timeout_us), _stream(stream)))
 
 
 def rf_attn_fwd(q, k, v, o, lse=None, scale=None, causal=False, stream=None):
@@ -331,11 +340,63 @@ def layernorm(x, residual, gamma, beta, eps=1e-5, want_residual_out=False, strea
     return (out, rout) if want_residual_out else out
 
 
+LN_VARIANTS = {0: "fused incremental", 1: "fused non-incremental (row in shared memory)",
+               2: "reductions fused, normalise separate", 3: "unfused"}
+XENT_VARIANTS = {0: "fused incremental", 1: "fused two-pass", 2: "unfused"}
+
+
+def rf_ablation_workspace_bytes(op, variant, rows, cols, dtype) -> int:
+    """Workspace bytes of an ablation variant (op 0 = LayerNorm, 1 = cross-entropy)."""
+    n = load().rf_ablation_workspace_bytes(int(op), int(variant), int(rows), int(cols), _code(dtype))
+    if n == ctypes.c_size_t(-1).value:
+        raise RFError(RF_ERR_INVALID_ARG, "rf_ablation_workspace_bytes: invalid arguments")
+    return n
+
+
+def rf_layernorm_ablation(x, residual, gamma, beta, out, variant, workspace=None, eps=1e-5, stream=None):
+    """LayerNorm(x + residual) * gamma + beta computed by ablation `variant` (see LN_VARIANTS)."""
+    rows, cols = x.shape
+    for name, t in (("residual", residual), ("out", out)):
+        if t is None or tuple(t.shape) != (rows, cols) or t.dtype != x.dtype:
+            raise ValueError(f"{name} must match x")
+    for name, t in (("gamma", gamma), ("beta", beta)):
+        if t is None or t.numel() != cols or t.dtype != x.dtype:
+            raise ValueError(f"{name} must hold cols elements of x's dtype")
+    wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().rf_layernorm_ablation(_dev(x, "x"), _dev(residual, "residual"), _dev(gamma, "gamma"),
+                                        _dev(beta, "beta"), _dev(out, "out"), rows, cols, float(eps), int(variant),
+                                        _dev(workspace, "workspace", True), wsb, _code(x.dtype), _stream(stream)))
+
+
+def rf_softmax_xent_ablation(logits, targets, loss, lse, variant, workspace=None, ignore_index=-100, stream=None):
+    """Cross-entropy loss (and lse) computed by ablation `variant` (see XENT_VARIANTS)."""
+    rows, V = logits.shape
+    if targets.dtype != torch.int64 or targets.numel() != rows:
+        raise ValueError("targets must be int64 with rows elements")
+    for name, t in (("loss", loss), ("lse", lse)):
+        if t is not None and (t.dtype != torch.float32 or t.numel() != rows):
+            raise ValueError(f"{name} must be float32 with rows elements")
+    wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().rf_softmax_xent_ablation(_dev(logits, "logits"), _dev(targets, "targets"), _dev(loss, "loss"),
+                                           _dev(lse, "lse", True), rows, V, int(ignore_index), int(variant),
+                                           _dev(workspace, "workspace", True), wsb, _code(logits.dtype),
+                                           _stream(stream)))
+
+
+def ablation_workspace(op, variant, rows, cols, dtype, device="cuda"):
+    """A device workspace (uint8) large enough for the variant, or None when it needs none."""
+    n = rf_ablation_workspace_bytes(op, variant, rows, cols, dtype)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+
+
 __all__ = [
-    "RFError", "load", "declared_symbols", "rf_version", "rf_last_error", "rf_device_status", "rf_attn_fwd",
+    "RFError", "load", "declared_symbols", "rf_version", "rf_last_error", "rf_device_status",
+    "rf_selftest_wait_timeout", "rf_attn_fwd",
     "rf_attn_fwd_ex", "AttnOpts", "alibi_slopes",
     "rf_attn_decode_splitkv_workspace_bytes", "rf_attn_decode_splitkv", "rf_attn_decode_splitkv_noalloc",
     "rf_lse_merge", "rf_layernorm_fused", "rf_rmsnorm_fused", "rmsnorm", "rf_softmax_xent", "softmax_xent",
     "attention", "decode", "decode_workspace", "decode_partials_view", "layernorm",
+    "rf_ablation_workspace_bytes", "rf_layernorm_ablation", "rf_softmax_xent_ablation", "ablation_workspace",
+    "LN_VARIANTS", "XENT_VARIANTS",
     "RF_OK", "RF_ERR_INVALID_ARG", "RF_ERR_UNSUPPORTED", "RF_ERR_CUDA", "RF_ERR_TIMEOUT",
 ]

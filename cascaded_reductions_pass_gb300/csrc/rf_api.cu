@@ -342,6 +342,16 @@ rf_status_t rf_layernorm_fused(const void* x, const void* residual, const void* 
                   "rf_layernorm_fused");
 }
 
+rf_status_t rf_selftest_wait_timeout(unsigned timeout_us, void* stream) {
+  if (timeout_us == 0 || timeout_us > 1000000u)
+    return fail(RF_ERR_INVALID_ARG, "rf_selftest_wait_timeout: timeout_us must be in [1, 1000000]");
+  unsigned* st = rf::device_status_ptr();
+  if (!st) return fail(RF_ERR_CUDA, "rf_selftest_wait_timeout: cannot resolve the device status word");
+  return launched(rf::launch_wait_timeout_selftest(uint64_t(timeout_us) * 1000u, st, nullptr,
+                                                   static_cast<cudaStream_t>(stream)),
+                  "rf_selftest_wait_timeout");
+}
+
 rf_status_t rf_softmax_xent(const void* logits, const long long* targets, float* loss, float* lse, void* grad,
                             int rows, int vocab, long long ignore_index, rf_dtype_t dtype, void* stream) {
   if (!logits || !targets || !loss)
@@ -388,6 +398,87 @@ rf_status_t rf_rmsnorm_fused(const void* x, const void* residual, const void* ga
   return launched(rf::launch_rmsnorm(x, residual, gamma, out, residual_out, rows, cols, eps,
                                      static_cast<rf::Dt>(dtype), static_cast<cudaStream_t>(stream)),
                   "rf_rmsnorm_fused");
+}
+
+size_t rf_ablation_workspace_bytes(int op, int variant, int rows, int cols, rf_dtype_t dtype) {
+  if (rows <= 0 || cols <= 0 || !valid_dtype(dtype)) return static_cast<size_t>(-1);
+  if (op == 0 && variant >= 0 && variant <= 3)
+    return rf::ablation_ln_workspace_bytes(rows, cols, variant, static_cast<rf::Dt>(dtype));
+  if (op == 1 && variant >= 0 && variant <= 2) return rf::ablation_xent_workspace_bytes(rows, variant);
+  return static_cast<size_t>(-1);
+}
+
+rf_status_t rf_layernorm_ablation(const void* x, const void* residual, const void* gamma, const void* beta,
+                                  void* out, int rows, int cols, float eps, int variant, void* workspace,
+                                  size_t workspace_bytes, rf_dtype_t dtype, void* stream) {
+  if (variant < 0 || variant > 3)
+    return fail(RF_ERR_INVALID_ARG, "rf_layernorm_ablation: variant=%d must be 0..3", variant);
+  if (!residual || !gamma || !beta)
+    return fail(RF_ERR_INVALID_ARG, "rf_layernorm_ablation: residual, gamma and beta are required");
+  if (variant == 0)
+    return rf_layernorm_fused(x, residual, gamma, beta, out, nullptr, rows, cols, eps, dtype, stream);
+  if (!x || !out) return fail(RF_ERR_INVALID_ARG, "rf_layernorm_ablation: x and out must be non-null");
+  if (rows <= 0 || cols <= 0) return fail(RF_ERR_INVALID_ARG, "rf_layernorm_ablation: sizes must be positive");
+  if (!(eps >= 0.0f) || !std::isfinite(eps))
+    return fail(RF_ERR_INVALID_ARG, "rf_layernorm_ablation: eps must be finite and >= 0");
+  if (!valid_dtype(dtype)) return fail(RF_ERR_INVALID_ARG, "rf_layernorm_ablation: unknown dtype %d", int(dtype));
+  if (!aligned16(x) || !aligned16(residual) || !aligned16(gamma) || !aligned16(beta) || !aligned16(out) ||
+      !aligned16(workspace))
+    return fail(RF_ERR_INVALID_ARG, "rf_layernorm_ablation: pointers must be 16-byte aligned");
+  const int vec = dtype == RF_F32 ? 4 : 8;
+  if (cols % vec != 0)
+    return fail(RF_ERR_INVALID_ARG, "rf_layernorm_ablation: cols=%d must be a multiple of %d for %s", cols, vec,
+                dt_name(dtype));
+  if (variant == 1 && cols > rf::kLnSmemMaxCols)
+    return fail(RF_ERR_UNSUPPORTED, "rf_layernorm_ablation: cols=%d exceeds %d for the shared-memory variant",
+                cols, rf::kLnSmemMaxCols);
+  const size_t need = rf::ablation_ln_workspace_bytes(rows, cols, variant, static_cast<rf::Dt>(dtype));
+  if (need && (!workspace || workspace_bytes < need))
+    return fail(RF_ERR_INVALID_ARG, "rf_layernorm_ablation: workspace of %zu bytes needed, %zu given", need,
+                workspace ? workspace_bytes : size_t(0));
+  RF_TRY(check_dev_ptr(x, "x"));
+  RF_TRY(check_dev_ptr(residual, "residual"));
+  RF_TRY(check_dev_ptr(gamma, "gamma"));
+  RF_TRY(check_dev_ptr(beta, "beta"));
+  RF_TRY(check_dev_ptr(out, "out"));
+  RF_TRY(check_dev_ptr(workspace, "workspace"));
+  return launched(rf::launch_ln_ablation(x, residual, gamma, beta, out, rows, cols, eps, variant, workspace,
+                                         static_cast<rf::Dt>(dtype), static_cast<cudaStream_t>(stream)),
+                  "rf_layernorm_ablation");
+}
+
+rf_status_t rf_softmax_xent_ablation(const void* logits, const long long* targets, float* loss, float* lse,
+                                     int rows, int vocab, long long ignore_index, int variant, void* workspace,
+                                     size_t workspace_bytes, rf_dtype_t dtype, void* stream) {
+  if (variant < 0 || variant > 2)
+    return fail(RF_ERR_INVALID_ARG, "rf_softmax_xent_ablation: variant=%d must be 0..2", variant);
+  if (variant == 0)
+    return rf_softmax_xent(logits, targets, loss, lse, nullptr, rows, vocab, ignore_index, dtype, stream);
+  if (!logits || !targets || !loss)
+    return fail(RF_ERR_INVALID_ARG, "rf_softmax_xent_ablation: logits, targets and loss must be non-null");
+  if (rows <= 0 || vocab <= 0)
+    return fail(RF_ERR_INVALID_ARG, "rf_softmax_xent_ablation: sizes must be positive");
+  if (!valid_dtype(dtype))
+    return fail(RF_ERR_INVALID_ARG, "rf_softmax_xent_ablation: unknown dtype %d", int(dtype));
+  if (!aligned16(logits) || !aligned16(workspace))
+    return fail(RF_ERR_INVALID_ARG, "rf_softmax_xent_ablation: logits and workspace must be 16-byte aligned");
+  const int vec = dtype == RF_F32 ? 4 : 8;
+  if (vocab % vec != 0)
+    return fail(RF_ERR_INVALID_ARG, "rf_softmax_xent_ablation: vocab=%d must be a multiple of %d for %s", vocab,
+                vec, dt_name(dtype));
+  const size_t need = rf::ablation_xent_workspace_bytes(rows, variant);
+  if (need && (!workspace || workspace_bytes < need))
+    return fail(RF_ERR_INVALID_ARG, "rf_softmax_xent_ablation: workspace of %zu bytes needed, %zu given", need,
+                workspace ? workspace_bytes : size_t(0));
+  RF_TRY(check_dev_ptr(logits, "logits"));
+  RF_TRY(check_dev_ptr(targets, "targets"));
+  RF_TRY(check_dev_ptr(loss, "loss"));
+  RF_TRY(check_dev_ptr(lse, "lse"));
+  RF_TRY(check_dev_ptr(workspace, "workspace"));
+  return launched(rf::launch_xent_ablation(logits, targets, loss, lse, rows, vocab, ignore_index, variant,
+                                           workspace, static_cast<rf::Dt>(dtype),
+                                           static_cast<cudaStream_t>(stream)),
+                  "rf_softmax_xent_ablation");
 }
 
 }  // extern "C"

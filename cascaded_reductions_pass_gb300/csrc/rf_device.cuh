@@ -213,6 +213,15 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, unsigned parity) {
       : "memory");
   return ok != 0;
 }
+// Wait for the phase with the given parity to complete; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, unsigned parity, uint64_t limit_ns) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > limit_ns) return false;
+  }
+  return true;
+}
 // Wait for the phase with the given parity to complete; false after RF_WAIT_NS.
 // A completed phase is seen by the non-blocking test (the blocking try_wait
 // costs ~100 cycles even then); otherwise poll try_wait against the timer.

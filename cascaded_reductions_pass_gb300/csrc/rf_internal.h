@@ -45,6 +45,18 @@ cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* o,
                            int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal,
                            int window, const float* alibi, Dt dt, unsigned* status, cudaStream_t s);
 
+// bounded-wait failure path self-test (selftest.cu)
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, unsigned* status, int* waited_out, cudaStream_t s);
+
+// fusion-level / incremental-form ablation variants (ablation.cu)
+constexpr int kLnSmemMaxCols = 56832;  // variant 1 stages cols floats in shared memory
+size_t ablation_ln_workspace_bytes(int rows, int cols, int variant, Dt dt);
+size_t ablation_xent_workspace_bytes(int rows, int variant);
+cudaError_t launch_ln_ablation(const void* x, const void* r, const void* g, const void* b, void* out, int rows,
+                               int cols, float eps, int variant, void* ws, Dt dt, cudaStream_t s);
+cudaError_t launch_xent_ablation(const void* logits, const long long* targets, float* loss, float* lse, int rows,
+                                 int vocab, long long ignore, int variant, void* ws, Dt dt, cudaStream_t s);
+
 // TMA descriptor encoding through the driver entry point (rf_api.cu).
 // 3-D tensor [outer][rows][inner] of 16-bit elements, box {64, box_rows, 1},
 // 128-byte swizzle; returns false (and sets *err) on failure.

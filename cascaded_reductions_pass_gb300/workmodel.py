@@ -58,3 +58,32 @@ def layernorm_bytes(rows, cols, dtype, affine=True, residual_out=False):
 def xent_bytes(rows, vocab, dtype, with_lse=True):
     """Logits read once, int64 targets read, fp32 loss (and LSE) written once."""
     return rows * vocab * ELEM_BYTES[dtype] + rows * 8 + rows * 4 + (rows * 4 if with_lse else 0)
+
+
+def ablation_bytes(op, variant, rows, cols, dtype):
+    """Compulsory HBM traffic of each ablation variant (RedFuser, Figure 7: a
+    level that is not fused into the one before re-reads that level's input).
+
+    op "layernorm" (cols = row length; t = one [rows, cols] tensor):
+      0, 1  x and r read once, y written once: 3t (+ gamma, beta)
+      2     statistics read x, r; normalise reads x, r again and writes y: 5t
+            (+ the per-row (mean, rstd) written and read back)
+      3     h = x + r written, read by the mean, variance and normalise
+            kernels: 2t + t + t + t + 2t = 7t (+ per-row statistics)
+    op "xent" (cols = vocab; T = the logits):
+      0     T read once
+      1     the row is read twice by one CTA: 2T through the memory system,
+            of which the second pass may be served by L2
+      2     the max and sum-of-exponentials kernels each read T: 2T
+    The small per-row vectors (targets, loss, lse, statistics) are included.
+    """
+    e = ELEM_BYTES[dtype]
+    if op == "layernorm":
+        t = rows * cols * e
+        aff = 2 * cols * e
+        return {0: 3 * t, 1: 3 * t, 2: 5 * t + 16 * rows, 3: 7 * t + 24 * rows}[variant] + aff
+    if op == "xent":
+        T = rows * cols * e
+        small = rows * 8 + rows * 8  # int64 targets; fp32 loss and lse
+        return {0: T, 1: 2 * T, 2: 2 * T + rows * 16}[variant] + small
+    raise ValueError(op)

@@ -287,6 +287,61 @@ int rf_version(void);
  */
 rf_status_t rf_device_status(void* stream, int clear);
 
+/*
+ * rf_selftest_wait_timeout -- exercise the failure path of the bounded
+ * device-side waits: launch one warp that waits on a barrier nothing signals,
+ * gives up after timeout_us microseconds (1 .. 1,000,000), and records
+ * RF_ERR_TIMEOUT in the device status word, as a production kernel does when
+ * one of its waits runs out.  No copy or tensor-memory allocation is in flight
+ * when it gives up, so the context stays usable.  A following
+ * rf_device_status() returns RF_ERR_TIMEOUT (and clears it when asked).
+ * Errors: RF_ERR_INVALID_ARG for a timeout out of range; RF_ERR_CUDA if the
+ * launch fails.
+ */
+rf_status_t rf_selftest_wait_timeout(unsigned timeout_us, void* stream);
+
+/*
+ * Ablation variants of the fused cascades (RedFuser, Figure 6: (a) fusion at
+ * different levels, (b) incremental vs non-incremental computation; Figure 7:
+ * what each level of fusion saves in re-reads).  These entry points exist to
+ * measure what the fused incremental kernels gain; they compute the same
+ * results, differing only in rounding order.
+ *
+ * rf_layernorm_ablation -- residual + LayerNorm as rf_layernorm_fused (x,
+ * residual, gamma, beta all required; no residual_out) with `variant`:
+ *   0  fused, incremental: rf_layernorm_fused itself (one read of x and r).
+ *   1  fused, non-incremental: one CTA per row stages h = x + r in shared
+ *      memory (cols * 4 bytes of on-chip memory), then a mean pass, a
+ *      variance pass and a normalise pass over it.  cols <= 56,832.
+ *   2  reductions fused, normalise separate: one kernel reads x and r for
+ *      (mean, rstd) per row; a second kernel reads x and r again to normalise.
+ *   3  unfused: h = x + r written to HBM, then a mean kernel, a variance kernel
+ *      and a normalise kernel, each reading h from HBM.
+ * rf_softmax_xent_ablation -- loss (and lse) as rf_softmax_xent without the
+ * gradient, with `variant`:
+ *   0  fused, incremental: rf_softmax_xent itself (one read of the logits).
+ *   1  fused, two-pass: one CTA per row reads the row for the max, then again
+ *      for sum exp(z - max) (level 2 waits for all of level 1; the row would
+ *      not fit on chip at vocabulary sizes, so the second pass re-reads it).
+ *   2  unfused: a max kernel, a sum-of-exponentials kernel and a loss kernel.
+ *
+ * `workspace` is device memory of at least rf_ablation_workspace_bytes(op,
+ * variant, rows, cols, dtype) bytes (op 0 = LayerNorm, 1 = cross-entropy;
+ * cols = vocab for op 1), 256-byte aligned, owned by the caller; nullable
+ * when that size is 0.  rf_ablation_workspace_bytes returns 0 for a variant
+ * that needs none and (size_t)-1 for invalid arguments.
+ * Errors: as the fused entry points, plus RF_ERR_INVALID_ARG for an unknown
+ * variant or a missing/short workspace and RF_ERR_UNSUPPORTED for a row too
+ * long for variant 1's shared memory.
+ */
+size_t rf_ablation_workspace_bytes(int op, int variant, int rows, int cols, rf_dtype_t dtype);
+rf_status_t rf_layernorm_ablation(const void* x, const void* residual, const void* gamma, const void* beta,
+                                  void* out, int rows, int cols, float eps, int variant, void* workspace,
+                                  size_t workspace_bytes, rf_dtype_t dtype, void* stream);
+rf_status_t rf_softmax_xent_ablation(const void* logits, const long long* targets, float* loss, float* lse,
+                                     int rows, int vocab, long long ignore_index, int variant, void* workspace,
+                                     size_t workspace_bytes, rf_dtype_t dtype, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -176,3 +176,57 @@ def test_attn_ex_rejects(lib):
     assert call(AttnOpts(0, 0, 0x10000)) == rf.RF_ERR_UNSUPPORTED
     assert call(AttnOpts(1, 16, None), Nk=9) == rf.RF_ERR_UNSUPPORTED and "Nq == Nk" in lib.rf_last_error().decode()
     assert call(AttnOpts(1, 16, 0x10002)) == rf.RF_ERR_INVALID_ARG and "aligned" in lib.rf_last_error().decode()
+
+
+def test_ablation_workspace_bytes(lib):
+    f = lib.rf_ablation_workspace_bytes
+    bad = ctypes.c_size_t(-1).value
+    assert f(0, 0, 64, 4096, 2) == 0 and f(0, 1, 64, 4096, 2) == 0
+    assert f(0, 2, 64, 4096, 2) == 64 * 8  # (mean, rstd) per row
+    # mean + (mean, rstd) per row, rounded to 256 bytes, then h [rows, cols] in the input dtype
+    assert f(0, 3, 64, 4096, 2) == 768 + 64 * 4096 * 2
+    assert f(0, 3, 64, 4096, 0) == 768 + 64 * 4096 * 4
+    assert f(1, 0, 16, 1024, 2) == 0 and f(1, 1, 16, 1024, 2) == 0 and f(1, 2, 16, 1024, 2) == 16 * 8
+    for args in ((0, 4, 8, 8, 2), (1, 3, 8, 8, 2), (2, 0, 8, 8, 2), (0, 0, 0, 8, 2), (0, 0, 8, 8, 7)):
+        assert f(*args) == bad
+
+
+@pytest.mark.parametrize("kw, status, msg", [
+    (dict(variant=4), rf.RF_ERR_INVALID_ARG, "variant"),
+    (dict(variant=-1), rf.RF_ERR_INVALID_ARG, "variant"),
+    (dict(residual=None), rf.RF_ERR_INVALID_ARG, "required"),
+    (dict(beta=None), rf.RF_ERR_INVALID_ARG, "required"),
+    (dict(variant=1, cols=56840), rf.RF_ERR_UNSUPPORTED, "shared-memory"),
+    (dict(variant=2, ws=None), rf.RF_ERR_INVALID_ARG, "workspace"),
+    (dict(variant=3, wsb=100), rf.RF_ERR_INVALID_ARG, "workspace"),
+    (dict(variant=2, x=MIS), rf.RF_ERR_INVALID_ARG, "aligned"),
+    (dict(variant=2, cols=12), rf.RF_ERR_INVALID_ARG, "multiple of 8"),
+    (dict(variant=2, eps=-1.0), rf.RF_ERR_INVALID_ARG, "eps"),
+    (dict(variant=0, cols=12), rf.RF_ERR_INVALID_ARG, "rf_layernorm_fused"),
+])
+def test_layernorm_ablation_rejects(lib, kw, status, msg):
+    a = dict(x=P, residual=P, gamma=P, beta=P, out=P, rows=4, cols=64, eps=1e-5, variant=2, ws=P, wsb=1 << 20,
+             dtype=2)
+    a.update(kw)
+    st = lib.rf_layernorm_ablation(a["x"], a["residual"], a["gamma"], a["beta"], a["out"], a["rows"], a["cols"],
+                                   a["eps"], a["variant"], a["ws"], a["wsb"], a["dtype"], S)
+    assert st == status
+    assert msg in lib.rf_last_error().decode()
+
+
+@pytest.mark.parametrize("kw, status, msg", [
+    (dict(variant=3), rf.RF_ERR_INVALID_ARG, "variant"),
+    (dict(variant=2, ws=None), rf.RF_ERR_INVALID_ARG, "workspace"),
+    (dict(variant=2, wsb=8), rf.RF_ERR_INVALID_ARG, "workspace"),
+    (dict(variant=1, logits=MIS), rf.RF_ERR_INVALID_ARG, "aligned"),
+    (dict(variant=1, vocab=100), rf.RF_ERR_INVALID_ARG, "multiple of 8"),
+    (dict(variant=1, loss=None), rf.RF_ERR_INVALID_ARG, "non-null"),
+    (dict(variant=0, rows=0), rf.RF_ERR_INVALID_ARG, "rf_softmax_xent"),
+])
+def test_softmax_xent_ablation_rejects(lib, kw, status, msg):
+    a = dict(logits=P, targets=P, loss=P, lse=None, rows=4, vocab=64, variant=2, ws=P, wsb=1 << 20, dtype=2)
+    a.update(kw)
+    st = lib.rf_softmax_xent_ablation(a["logits"], a["targets"], a["loss"], a["lse"], a["rows"], a["vocab"], -100,
+                                      a["variant"], a["ws"], a["wsb"], a["dtype"], S)
+    assert st == status
+    assert msg in lib.rf_last_error().decode()
