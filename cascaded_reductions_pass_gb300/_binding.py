@@ -33,11 +33,13 @@ _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_
 
 
 class AttnOpts(ctypes.Structure):
-    """rf_attn_opts_t: causal mask, sliding window, ALiBi slopes (device fp32 [Hq])."""
-    _fields_ = [("causal", ctypes.c_int), ("window", ctypes.c_int), ("alibi_slopes", ctypes.c_void_p)]
+    """rf_attn_opts_t: causal mask, sliding window, ALiBi slopes (device fp32 [Hq]), split-tail workspace."""
+    _fields_ = [("causal", ctypes.c_int), ("window", ctypes.c_int), ("alibi_slopes", ctypes.c_void_p),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
 _SIGNATURES = {
     "rf_attn_fwd": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp], _i),
     "rf_attn_fwd_ex": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, ctypes.POINTER(AttnOpts), _i, _vp], _i),
+    "rf_attn_fwd_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i], _sz),
     "rf_attn_decode_splitkv_workspace_bytes": ([_i, _i, _i, _i], _sz),
     "rf_attn_decode_splitkv": ([_vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _i, _f, _i, _vp], _i),
     "rf_attn_decode_splitkv_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp], _i),
@@ -153,9 +155,11 @@ def rf_attn_fwd(q, k, v, o, lse=None, scale=None, causal=False, stream=None):
                               B, Hq, Hkv, Nq, Nk, D, scale, int(bool(causal)), _code(q.dtype), _stream(stream)))
 
 
-def rf_attn_fwd_ex(q, k, v, o, lse=None, scale=None, causal=False, window=0, alibi_slopes=None, stream=None):
+def rf_attn_fwd_ex(q, k, v, o, lse=None, scale=None, causal=False, window=0, alibi_slopes=None, workspace=None,
+                   stream=None):
     """rf_attn_fwd with a sliding window (key j visible iff i - window < j <= i) and/or
-    ALiBi slopes (float32 CUDA tensor [Hq]); both need causal=True."""
+    ALiBi slopes (float32 CUDA tensor [Hq]), both needing causal=True, and an optional
+    workspace (uint8 CUDA tensor, see attn_workspace) for splitting a short last wave."""
     B, Hq, Nq, D = q.shape
     Hkv, Nk = k.shape[1], k.shape[2]
     if tuple(k.shape) != (B, Hkv, Nk, D) or tuple(v.shape) != tuple(k.shape) or tuple(o.shape) != tuple(q.shape):
@@ -167,9 +171,27 @@ def rf_attn_fwd_ex(q, k, v, o, lse=None, scale=None, causal=False, window=0, ali
     if alibi_slopes is not None and (alibi_slopes.dtype != torch.float32 or alibi_slopes.numel() != Hq):
         raise ValueError("alibi_slopes must be float32 with Hq elements")
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
-    opts = AttnOpts(int(bool(causal)), int(window), _dev(alibi_slopes, "alibi_slopes", True))
+    wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    opts = AttnOpts(int(bool(causal)), int(window), _dev(alibi_slopes, "alibi_slopes", True),
+                    _dev(workspace, "workspace", True), wsb)
     _check(load().rf_attn_fwd_ex(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(o, "o"), _dev(lse, "lse", True),
                                  B, Hq, Hkv, Nq, Nk, D, scale, ctypes.byref(opts), _code(q.dtype), _stream(stream)))
+
+
+def rf_attn_fwd_workspace_bytes(B, Hq, Nq, Nk, D, causal, dtype) -> int:
+    """Workspace bytes rf_attn_fwd_ex can use on the current device (0: nothing to split)."""
+    n = load().rf_attn_fwd_workspace_bytes(int(B), int(Hq), int(Nq), int(Nk), int(D), int(bool(causal)),
+                                           _code(dtype))
+    if n == ctypes.c_size_t(-1).value:
+        raise RFError(RF_ERR_INVALID_ARG, "rf_attn_fwd_workspace_bytes: invalid arguments or no device")
+    return n
+
+
+def attn_workspace(q, k, causal=False):
+    """A uint8 workspace for rf_attn_fwd_ex's split tail, or None when nothing would be split."""
+    B, Hq, Nq, D = q.shape
+    n = rf_attn_fwd_workspace_bytes(B, Hq, Nq, k.shape[2], D, causal, q.dtype)
+    return torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
 
 
 def rf_attn_decode_splitkv_workspace_bytes(B, Hq, D, num_splits) -> int:
@@ -280,15 +302,16 @@ def alibi_slopes(n_heads, device="cuda"):
 
 
 # ------------------------------------------------------------------ allocating helpers
-def attention(q, k, v, scale=None, causal=False, window=0, alibi_slopes=None, stream=None):
-    """Allocate (o, lse) and run rf_attn_fwd (rf_attn_fwd_ex for a window or ALiBi)."""
+def attention(q, k, v, scale=None, causal=False, window=0, alibi_slopes=None, split_tail=True, stream=None):
+    """Allocate (o, lse) and run rf_attn_fwd_ex; with split_tail (the default) a short last
+    wave of the unmasked 16-bit kernel is split along the keys (a workspace is allocated)."""
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
-    if window or alibi_slopes is not None:
-        rf_attn_fwd_ex(q, k, v, o, lse, scale=scale, causal=causal, window=window, alibi_slopes=alibi_slopes,
-                       stream=stream)
-    else:
-        rf_attn_fwd(q, k, v, o, lse, scale=scale, causal=causal, stream=stream)
+    ws = None
+    if split_tail and not causal and q.dtype != torch.float32:
+        ws = attn_workspace(q, k, causal)
+    rf_attn_fwd_ex(q, k, v, o, lse, scale=scale, causal=causal, window=window, alibi_slopes=alibi_slopes,
+                   workspace=ws, stream=stream)
     return o, lse
 
 
@@ -392,7 +415,7 @@ def ablation_workspace(op, variant, rows, cols, dtype, device="cuda"):
 __all__ = [
     "RFError", "load", "declared_symbols", "rf_version", "rf_last_error", "rf_device_status",
     "rf_selftest_wait_timeout", "rf_attn_fwd",
-    "rf_attn_fwd_ex", "AttnOpts", "alibi_slopes",
+    "rf_attn_fwd_ex", "AttnOpts", "alibi_slopes", "rf_attn_fwd_workspace_bytes", "attn_workspace",
     "rf_attn_decode_splitkv_workspace_bytes", "rf_attn_decode_splitkv", "rf_attn_decode_splitkv_noalloc",
     "rf_lse_merge", "rf_layernorm_fused", "rf_rmsnorm_fused", "rmsnorm", "rf_softmax_xent", "softmax_xent",
     "attention", "decode", "decode_workspace", "decode_partials_view", "layernorm",

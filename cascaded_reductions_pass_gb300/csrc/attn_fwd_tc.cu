@@ -40,11 +40,20 @@
 // K-major (boxes of 64 dims x 128 rows), V MN-major (the same boxes read as
 // D x keys).  Causal CTAs are scheduled longest-first, and the query heads of
 // one GQA group are adjacent in launch order so their K/V tiles hit in L2.
+//
+// Split tail (no mask, caller workspace given): with one CTA per SM, U units
+// of 256 query rows take ceil(U / SMs) waves, and a last wave of a few units
+// leaves most SMs idle for a whole unit.  The last U mod SMs units are then
+// split along the keys into n_split pieces each (one CTA per piece), which
+// write their normalised partial O_s and lse_s in fp32 to the workspace; the
+// log-sum-exp merge (RedFuser, Figure 13: the FlashDecoding split and merge)
+// then writes those rows of O and LSE.
 // Every mbarrier wait is bounded; on a timeout the CTA records RF_ERR_TIMEOUT,
 // waits (bounded) for its copies and MMAs in flight, frees TMEM and exits.
 #include <cuda.h>
 #include <math.h>
 
+#include "lse_merge.cuh"
 #include "rf_device.cuh"
 
 namespace rf {
@@ -80,6 +89,25 @@ struct alignas(8) TcBars {
   int abort;
 };
 
+// Unit (CTA of whole rows) id -> query-tile pair c and batch*head bh: the
+// longest causal units first, the heads of one GQA group adjacent.
+__host__ __device__ __forceinline__ void unit_coords(int id, int BH, int nqt, int& c, int& bh) {
+  c = nqt - 1 - id / BH;
+  bh = id - (id / BH) * BH;
+}
+
+// Output rows of the split tail's partial rows (partial row g = row g % 256 of
+// tail unit g / 256); rows past Nq are skipped.
+struct AttnTailRows {
+  int first_unit, BH, nqt, Nq;
+  __device__ __forceinline__ long long operator()(long long g) const {
+    int c, bh;
+    unit_coords(first_unit + static_cast<int>(g / (2 * kBM)), BH, nqt, c, bh);
+    const int q = c * 2 * kBM + static_cast<int>(g % (2 * kBM));
+    return q < Nq ? static_cast<long long>(bh) * Nq + q : -1;
+  }
+};
+
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, unsigned parity) {
   const bool ok = mbar_wait(bar, parity);
   return __all_sync(0xffffffffu, ok);
@@ -93,7 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, uint16_t* __restrict__ o, float* __restrict__ lse,
                    int Hq, int Hkv, int Nq, int Nk, int BH, int nqt, float sl2, int window,
-                   const float* __restrict__ alibi, unsigned* status) {
+                   const float* __restrict__ alibi, unsigned* status, int n_full, int n_split,
+                   float* __restrict__ o_part, float* __restrict__ lse_part) {
   constexpr bool CAUSAL = MASK >= 1;
   using C = Cfg<D>;
   constexpr int S = C::kStages;
@@ -106,19 +135,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   TcBars* bars = reinterpret_cast<TcBars*>(sV + S * C::kKVBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // CTAs from n_full on are pieces of the split tail: piece p is key range
+  // p % n_split of unit n_full + p / n_split.
   const int id = blockIdx.x;
-  const int c = nqt - 1 - id / BH;  // longest-first for causal
-  const int bh = id - (id / BH) * BH;
+  const bool piece = MASK == 0 && id >= n_full;
+  const int unit = piece ? n_full + (id - n_full) / n_split : id;
+  const int split = piece ? (id - n_full) % n_split : 0;
+  int c, bh;
+  unit_coords(unit, BH, nqt, c, bh);
   const int h = bh % Hq, b = bh / Hq;
   const int kv_plane = b * Hkv + h / (Hq / Hkv);
   const int r0 = c * 2 * kBM;
   // Key tiles [lo_t, nt_t) that query tile t can see; the CTA streams
   // [lo0, nt1) (tile 1's rows come after tile 0's, so lo0 <= lo1, nt0 <= nt1).
   const int n_kv = (Nk + kBN - 1) / kBN;
-  const int nt0 = CAUSAL ? min(r0 / kBN + 1, n_kv) : n_kv;
-  const int nt1 = CAUSAL ? min(r0 / kBN + 2, n_kv) : n_kv;
-  const int lo0 = MASK == 2 ? max(0, r0 - window + 1) / kBN : 0;
-  const int lo1 = MASK == 2 ? max(0, r0 + kBM - window + 1) / kBN : 0;
+  // a piece's key tiles: [floor(split n_kv / n_split), floor((split + 1) n_kv / n_split)), never empty
+  const int plo = piece ? static_cast<int>(static_cast<long long>(split) * n_kv / n_split) : 0;
+  const int phi = piece ? static_cast<int>(static_cast<long long>(split + 1) * n_kv / n_split) : n_kv;
+  const int nt0 = CAUSAL ? min(r0 / kBN + 1, n_kv) : phi;
+  const int nt1 = CAUSAL ? min(r0 / kBN + 2, n_kv) : phi;
+  const int lo0 = MASK == 2 ? max(0, r0 - window + 1) / kBN : plo;
+  const int lo1 = MASK == 2 ? max(0, r0 + kBM - window + 1) / kBN : plo;
   const int n_load = nt1 - lo0;
 
   if (threadIdx.x == 0) {
@@ -438,23 +475,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv = 1.0f / l_run;
       const bool row_ok = row < Nq;
-      uint4* orow = reinterpret_cast<uint4*>(o + (static_cast<long long>(bh) * Nq + (row_ok ? row : 0)) * D);
+      if (piece) {  // partial row g of the split tail: O_s and lse_s in fp32
+        const long long g = static_cast<long long>(unit - n_full) * (2 * kBM) + (row - r0);
+        float4* prow = reinterpret_cast<float4*>(o_part + (g * n_split + split) * D);
 #pragma unroll
-      for (int i = 0; i < D / 32; ++i) {
-        uint32_t ov[32];
-        tc_ld32(tO + 32 * i, ov);
-        tc_wait_ld();
-        uint32_t pk[16];
+        for (int i = 0; i < D / 32; ++i) {
+          uint32_t ov[32];
+          tc_ld32(tO + 32 * i, ov);
+          tc_wait_ld();
+          if (row_ok) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pk[e] = Pack<DT>::pack2(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
-        if (row_ok) {
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            orow[i * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+            for (int v4 = 0; v4 < 8; ++v4)
+              prow[i * 8 + v4] =
+                  make_float4(__uint_as_float(ov[4 * v4]) * inv, __uint_as_float(ov[4 * v4 + 1]) * inv,
+                              __uint_as_float(ov[4 * v4 + 2]) * inv, __uint_as_float(ov[4 * v4 + 3]) * inv);
+          }
         }
+        if (row_ok) lse_part[g * n_split + split] = (m_run + log2f(l_run)) * kLn2;
+      } else {
+        uint4* orow =
+            reinterpret_cast<uint4*>(o + (static_cast<long long>(bh) * Nq + (row_ok ? row : 0)) * D);
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) {
+          uint32_t ov[32];
+          tc_ld32(tO + 32 * i, ov);
+          tc_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = Pack<DT>::pack2(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
+          if (row_ok) {
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              orow[i * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          }
+        }
+        if (row_ok && lse) lse[static_cast<long long>(bh) * Nq + row] = (m_run + log2f(l_run)) * kLn2;
       }
-      if (row_ok && lse) lse[static_cast<long long>(bh) * Nq + row] = (m_run + log2f(l_run)) * kLn2;
     } else {
       if (lane == 0) atomicOr(status, kStatusTimeout);
       bars->abort = 1;
@@ -469,10 +526,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Split-tail plan: the last `tail` = units mod sms units become n_split pieces
+// each (n_split = min(sms / tail, key tiles) >= 2), else nothing is split.
+struct TailPlan {
+  long long n_full;
+  int tail, n_split;
+};
+
+TailPlan tail_plan(long long units, int n_kv, int sms) {
+  const int tail = sms > 0 ? static_cast<int>(units % sms) : 0;
+  const int n_split = tail > 0 ? min(sms / tail, n_kv) : 1;
+  if (tail == 0 || n_split < 2) return TailPlan{units, 0, 1};
+  return TailPlan{units - tail, tail, n_split};
+}
+
+// Workspace layout of a split tail: o_part [tail * 256, n_split, D] fp32, then
+// lse_part [tail * 256, n_split] fp32 at the next 256-byte boundary.
+size_t tail_o_bytes(const TailPlan& p, int D) {
+  return (static_cast<size_t>(p.tail) * 2 * kBM * p.n_split * D * sizeof(float) + 255) & ~size_t(255);
+}
+size_t tail_bytes(const TailPlan& p, int D) {
+  if (p.tail == 0) return 0;
+  return tail_o_bytes(p, D) + static_cast<size_t>(p.tail) * 2 * kBM * p.n_split * sizeof(float);
+}
+
+TailPlan plan_for(int B, int Hq, int Nq, int Nk, int sms) {
+  const long long units = static_cast<long long>((Nq + 2 * kBM - 1) / (2 * kBM)) * B * Hq;
+  return tail_plan(units, (Nk + kBN - 1) / kBN, sms);
+}
+
 template <Dt DT, int D, int MASK, bool ALIBI>
 cudaError_t launch_cfg(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                        int Nq, int Nk, float scale, int window, const float* alibi, unsigned* status,
-                       cudaStream_t s) {
+                       const TailPlan& plan, void* ws, cudaStream_t s) {
   alignas(64) CUtensorMap tq, tk, tv;
   cudaError_t err = cudaSuccess;
   if (!encode_tma_3d_16bit(&tq, q, D, Nq, uint64_t(B) * Hq, kBM, &err)) return err;
@@ -485,37 +571,58 @@ cudaError_t launch_cfg(const void* q, const void* k, const void* v, void* o, flo
   auto kern = attn_tc_kernel<DT, D, MASK, ALIBI>;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  kern<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(tq, tk, tv, static_cast<uint16_t*>(o), lse, Hq, Hkv, Nq,
-                                                           Nk, B * Hq, nqt, scale * kLog2e, window, alibi, status);
+  const bool split = MASK == 0 && plan.tail > 0 && ws != nullptr;
+  float* o_part = split ? static_cast<float*>(ws) : nullptr;
+  float* lse_part = split ? reinterpret_cast<float*>(static_cast<char*>(ws) + tail_o_bytes(plan, D)) : nullptr;
+  const long long n_full = split ? plan.n_full : grid;
+  const long long ctas = split ? plan.n_full + static_cast<long long>(plan.tail) * plan.n_split : grid;
+  kern<<<static_cast<unsigned>(ctas), kThreads, smem, s>>>(tq, tk, tv, static_cast<uint16_t*>(o), lse, Hq, Hkv, Nq,
+                                                           Nk, B * Hq, nqt, scale * kLog2e, window, alibi, status,
+                                                           static_cast<int>(n_full), split ? plan.n_split : 1,
+                                                           o_part, lse_part);
+  err = cudaGetLastError();
+  if (err != cudaSuccess || !split) return err;
+  const int rows = plan.tail * 2 * kBM;
+  const AttnTailRows map{static_cast<int>(plan.n_full), B * Hq, nqt, Nq};
+  lse_merge_kernel<DT><<<(rows + kMergeWarps - 1) / kMergeWarps, kMergeWarps * 32, 0, s>>>(
+      o_part, lse_part, o, lse, rows, plan.n_split, D, map);
   return cudaGetLastError();
 }
 
 template <Dt DT, int D>
 cudaError_t launch_d(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                      int Nq, int Nk, float scale, int causal, int window, const float* alibi, unsigned* status,
-                     cudaStream_t s) {
-  if (!causal) return launch_cfg<DT, D, 0, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, 0, nullptr, status, s);
+                     const TailPlan& plan, void* ws, cudaStream_t s) {
+  const TailPlan none{0, 0, 1};
+  if (!causal)
+    return launch_cfg<DT, D, 0, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, 0, nullptr, status, plan, ws, s);
   if (window > 0) {
-    return alibi ? launch_cfg<DT, D, 2, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, window, alibi, status, s)
-                 : launch_cfg<DT, D, 2, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, window, nullptr, status, s);
+    return alibi ? launch_cfg<DT, D, 2, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, window, alibi, status,
+                                              none, nullptr, s)
+                 : launch_cfg<DT, D, 2, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, window, nullptr, status,
+                                               none, nullptr, s);
   }
-  return alibi ? launch_cfg<DT, D, 1, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, 0, alibi, status, s)
-               : launch_cfg<DT, D, 1, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, 0, nullptr, status, s);
+  return alibi ? launch_cfg<DT, D, 1, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, 0, alibi, status, none,
+                                            nullptr, s)
+               : launch_cfg<DT, D, 1, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, 0, nullptr, status, none,
+                                             nullptr, s);
 }
 
 }  // namespace
 
+size_t attn_tc_workspace_bytes(int B, int Hq, int Nq, int Nk, int D, int causal, int sms) {
+  if (causal) return 0;
+  return tail_bytes(plan_for(B, Hq, Nq, Nk, sms), D);
+}
+
 cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                            int Nq, int Nk, int D, float scale, int causal, int window, const float* alibi, Dt dt,
-                           unsigned* status, cudaStream_t s) {
-  if (dt == Dt::BF16)
-    return D == 128
-               ? launch_d<Dt::BF16, 128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, alibi, status, s)
-               : launch_d<Dt::BF16, 64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, alibi, status, s);
-  if (dt == Dt::F16)
-    return D == 128
-               ? launch_d<Dt::F16, 128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, alibi, status, s)
-               : launch_d<Dt::F16, 64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, alibi, status, s);
+                           unsigned* status, void* ws, int sms, cudaStream_t s) {
+  const TailPlan plan = plan_for(B, Hq, Nq, Nk, sms);
+#define RF_ATTN_ARGS q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, alibi, status, plan, ws, s
+  if (dt == Dt::BF16) return D == 128 ? launch_d<Dt::BF16, 128>(RF_ATTN_ARGS) : launch_d<Dt::BF16, 64>(RF_ATTN_ARGS);
+  if (dt == Dt::F16) return D == 128 ? launch_d<Dt::F16, 128>(RF_ATTN_ARGS) : launch_d<Dt::F16, 64>(RF_ATTN_ARGS);
+#undef RF_ATTN_ARGS
   return cudaErrorNotSupported;
 }
 

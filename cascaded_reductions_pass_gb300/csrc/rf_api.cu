@@ -106,6 +106,26 @@ unsigned* device_status_ptr() {
   return ptrs[dev];
 }
 
+int device_sm_count() {
+  static std::mutex mu;
+  static int counts[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 0;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if (counts[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    counts[dev] = n;
+  }
+  return counts[dev];
+}
+
 bool encode_tma_3d_16bit(void* tmap_out, const void* base, uint64_t inner, uint64_t rows,
                          uint64_t outer, uint32_t box_rows, cudaError_t* err) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
@@ -175,7 +195,7 @@ namespace {
 
 rf_status_t attn_impl(const char* name, const void* q, const void* k, const void* v, void* o, float* lse, int B,
                       int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal, int window,
-                      const float* alibi, rf_dtype_t dtype, void* stream) {
+                      const float* alibi, void* ws, size_t ws_bytes, rf_dtype_t dtype, void* stream) {
   if (!q || !k || !v || !o) return fail(RF_ERR_INVALID_ARG, "%s: q, k, v and o must be non-null", name);
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || D <= 0)
     return fail(RF_ERR_INVALID_ARG, "%s: sizes must be positive (B=%d Hq=%d Hkv=%d Nq=%d Nk=%d D=%d)", name, B, Hq,
@@ -185,7 +205,7 @@ rf_status_t attn_impl(const char* name, const void* q, const void* k, const void
     return fail(RF_ERR_INVALID_ARG, "%s: scale must be finite and positive", name);
   if (!valid_dtype(dtype)) return fail(RF_ERR_INVALID_ARG, "%s: unknown dtype %d", name, int(dtype));
   if (window < 0) return fail(RF_ERR_INVALID_ARG, "%s: window must be >= 0", name);
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(ws))
     return fail(RF_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", name);
   if ((reinterpret_cast<uintptr_t>(alibi) & 3u) != 0)
     return fail(RF_ERR_INVALID_ARG, "%s: alibi_slopes must be 4-byte aligned", name);
@@ -206,6 +226,15 @@ rf_status_t attn_impl(const char* name, const void* q, const void* k, const void
   RF_TRY(check_dev_ptr(lse, "lse"));
   RF_TRY(check_dev_ptr(alibi, "alibi_slopes"));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int sms = 0;
+  if (ws && dtype != RF_F32 && !causal) {  // the split tail needs the workspace it is sized for
+    sms = rf::device_sm_count();
+    if (sms <= 0) return fail(RF_ERR_CUDA, "%s: cannot query the multiprocessor count", name);
+    const size_t need = rf::attn_tc_workspace_bytes(B, Hq, Nq, Nk, D, causal, sms);
+    if (ws_bytes < need)
+      return fail(RF_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", name, need, ws_bytes);
+    RF_TRY(check_dev_ptr(ws, "workspace"));
+  }
   if (dtype == RF_F32)
     return launched(rf::launch_attn_f32(static_cast<const float*>(q), static_cast<const float*>(k),
                                         static_cast<const float*>(v), static_cast<float*>(o), lse, B, Hq, Hkv, Nq, Nk,
@@ -214,7 +243,7 @@ rf_status_t attn_impl(const char* name, const void* q, const void* k, const void
   unsigned* st = rf::device_status_ptr();
   if (!st) return fail(RF_ERR_CUDA, "%s: cannot resolve the device status word", name);
   return launched(rf::launch_attn_tc(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi,
-                                     static_cast<rf::Dt>(dtype), st, s),
+                                     static_cast<rf::Dt>(dtype), st, sms > 0 ? ws : nullptr, sms, s),
                   name);
 }
 
@@ -224,8 +253,8 @@ extern "C" {
 
 rf_status_t rf_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                         int Nq, int Nk, int D, float scale, int causal, rf_dtype_t dtype, void* stream) {
-  return attn_impl("rf_attn_fwd", q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal ? 1 : 0, 0, nullptr, dtype,
-                   stream);
+  return attn_impl("rf_attn_fwd", q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal ? 1 : 0, 0, nullptr, nullptr,
+                   0, dtype, stream);
 }
 
 rf_status_t rf_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
@@ -234,8 +263,19 @@ rf_status_t rf_attn_fwd_ex(const void* q, const void* k, const void* v, void* o,
   const int causal = opts ? (opts->causal ? 1 : 0) : 0;
   const int window = opts ? opts->window : 0;
   const float* alibi = opts ? opts->alibi_slopes : nullptr;
-  return attn_impl("rf_attn_fwd_ex", q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi, dtype,
-                   stream);
+  void* ws = opts ? opts->workspace : nullptr;
+  const size_t ws_bytes = opts ? opts->workspace_bytes : 0;
+  return attn_impl("rf_attn_fwd_ex", q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi, ws,
+                   ws_bytes, dtype, stream);
+}
+
+size_t rf_attn_fwd_workspace_bytes(int B, int Hq, int Nq, int Nk, int D, int causal, rf_dtype_t dtype) {
+  if (B <= 0 || Hq <= 0 || Nq <= 0 || Nk <= 0 || D <= 0 || !valid_dtype(dtype)) return static_cast<size_t>(-1);
+  if (causal || dtype == RF_F32) return 0;
+  if (D != 64 && D != 128) return static_cast<size_t>(-1);
+  const int sms = rf::device_sm_count();
+  if (sms <= 0) return static_cast<size_t>(-1);
+  return rf::attn_tc_workspace_bytes(B, Hq, Nq, Nk, D, causal, sms);
 }
 
 size_t rf_attn_decode_splitkv_workspace_bytes(int B, int Hq, int D, int num_splits) {

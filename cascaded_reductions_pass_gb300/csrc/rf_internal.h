@@ -40,10 +40,18 @@ cudaError_t launch_decode_split(const void* q, const void* k, const void* v, flo
                                 float* lse_part, int B, int Hq, int Hkv, int L, int D, int splits,
                                 float scale, Dt dt, unsigned* status, cudaStream_t s);
 
-// tcgen05 / TMEM / TMA attention forward for 16-bit inputs (attn_fwd_tc.cu)
+// tcgen05 / TMEM / TMA attention forward for 16-bit inputs (attn_fwd_tc.cu).
+// Without a mask, and with `ws` non-null, the units of the last partial wave
+// on `sms` SMs are split along the keys and merged; ws must then hold
+// attn_tc_workspace_bytes(...) bytes (0 when nothing is split).
+size_t attn_tc_workspace_bytes(int B, int Hq, int Nq, int Nk, int D, int causal, int sms);
 cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* o, float* lse,
                            int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal,
-                           int window, const float* alibi, Dt dt, unsigned* status, cudaStream_t s);
+                           int window, const float* alibi, Dt dt, unsigned* status, void* ws, int sms,
+                           cudaStream_t s);
+
+// multiprocessor count of the current device (cached per device; 0 on error)
+int device_sm_count();
 
 // bounded-wait failure path self-test (selftest.cu)
 cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, unsigned* status, int* waited_out, cudaStream_t s);

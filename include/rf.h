@@ -94,19 +94,43 @@ rf_status_t rf_attn_fwd(const void* q, const void* k, const void* v, void* o, fl
  *                 Key tiles wholly outside every row's window are skipped.
  *   alibi_slopes  nullable device pointer to Hq fp32 slopes: slope[h]*(j - i)
  *                 is added to each scaled score (the linear-bias form of ALiBi).
+ *   workspace     nullable device memory of workspace_bytes bytes (16-byte
+ *                 aligned, owned by the caller, contents need not be set).
+ *                 Without a mask, the 16-bit kernel runs one CTA of 256 query
+ *                 rows per SM; when the last wave of such units is short, a
+ *                 workspace lets those units be split along the keys over the
+ *                 idle SMs and merged by a log-sum-exp combine (RedFuser,
+ *                 Figure 13: the FlashDecoding split and merge) in a second
+ *                 kernel on the same stream.  It needs
+ *                 rf_attn_fwd_workspace_bytes(...) bytes; a null workspace
+ *                 runs every unit whole (same results up to rounding order).
+ *                 Calls that overlap on the GPU must not share a workspace.
  * The window and ALiBi need the causal mask (RF_ERR_UNSUPPORTED otherwise).
  * The LSE output includes the ALiBi bias.  Everything else (layouts,
  * supported dtypes and head dims, errors) is as rf_attn_fwd; a negative window
- * is RF_ERR_INVALID_ARG.
+ * is RF_ERR_INVALID_ARG, and so is a workspace smaller than it needs to be.
  */
 typedef struct rf_attn_opts_t {
   int causal;
   int window;
   const float* alibi_slopes;
+  void* workspace;        /* nullable device memory, see rf_attn_fwd_workspace_bytes */
+  size_t workspace_bytes;
 } rf_attn_opts_t;
 rf_status_t rf_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
                            int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale,
                            const rf_attn_opts_t* opts, rf_dtype_t dtype, void* stream);
+
+/*
+ * rf_attn_fwd_workspace_bytes -- bytes of workspace that rf_attn_fwd_ex can
+ * use for the split of the last short wave on the current device (its
+ * multiprocessor count decides the split).  0 when nothing would be split:
+ * causal, fp32, a single key tile, or a last wave that is full or more than
+ * half full.  (size_t)-1 for invalid sizes, an unsupported D, or a device that
+ * cannot be queried.  At most 256 rows x (D + 1) x 4 bytes per multiprocessor
+ * (about 20 MiB on 152 SMs at D = 128).
+ */
+size_t rf_attn_fwd_workspace_bytes(int B, int Hq, int Nq, int Nk, int D, int causal, rf_dtype_t dtype);
 
 /*
  * rf_attn_decode_splitkv_workspace_bytes -- scratch size for rf_attn_decode_splitkv:

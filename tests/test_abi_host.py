@@ -230,3 +230,21 @@ def test_softmax_xent_ablation_rejects(lib, kw, status, msg):
                                       a["variant"], a["ws"], a["wsb"], a["dtype"], S)
     assert st == status
     assert msg in lib.rf_last_error().decode()
+
+
+def test_attn_workspace_bytes_host_cases(lib):
+    f = lib.rf_attn_fwd_workspace_bytes
+    bad = ctypes.c_size_t(-1).value
+    assert f(1, 8, 1024, 1024, 64, 1, 1) == 0  # causal: never split
+    assert f(1, 8, 1024, 1024, 64, 0, 0) == 0  # fp32 path: never split
+    assert f(0, 8, 1024, 1024, 64, 0, 1) == bad
+    assert f(1, 8, 1024, 1024, 96, 0, 1) == bad  # no tensor-core kernel for D=96
+    assert f(1, 8, 1024, 1024, 64, 0, 9) == bad
+
+
+def test_attn_ex_rejects_misaligned_workspace(lib):
+    from cascaded_reductions_pass_gb300._binding import AttnOpts
+
+    opts = AttnOpts(0, 0, None, 0x10008, 1 << 20)
+    st = lib.rf_attn_fwd_ex(P, P, P, P, None, 1, 2, 1, 8, 8, 64, 0.125, ctypes.byref(opts), 1, S)
+    assert st == rf.RF_ERR_INVALID_ARG and "aligned" in lib.rf_last_error().decode()

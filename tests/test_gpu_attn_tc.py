@@ -162,3 +162,65 @@ def test_variant_workloads_sampled(rf, name):
                                   alibi_slopes=slopes[h:h + 1] if slopes is not None else None)
         check16(o[b:b + 1, h:h + 1, rows].cpu(), ro, name)
         check_lse(lse[b:b + 1, h:h + 1, rows].cpu(), rl, what=name)
+
+
+# ---------------------------------------------------------------- split tail
+def expected_tail_plan(B, Hq, Nq, Nk, sms):
+    """Units of 256 query rows; the last units mod sms are split into min(sms // tail, key tiles) pieces."""
+    units = -(-Nq // 256) * B * Hq
+    tail = units % sms
+    n_split = min(sms // tail, -(-Nk // 128)) if tail else 1
+    return (tail, n_split) if tail and n_split >= 2 else (0, 1)
+
+
+def run_ex(rf, q, k, v, scale, workspace):
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    rf.rf_attn_fwd_ex(q, k, v, o, lse, scale=scale, workspace=workspace)
+    torch.cuda.synchronize()
+    return o.cpu(), lse.cpu()
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,D,dtype", [
+    (1, 8, 8, 1024, 1024, 64, "f16"),    # 32 units: all in the tail
+    (1, 1, 1, 256, 4096, 64, "bf16"),    # one unit split into one key tile per piece
+    (1, 3, 1, 300, 1000, 128, "bf16"),   # GQA, ragged query rows and keys
+    (2, 4, 2, 512, 640, 128, "f16"),
+])
+def test_split_tail_matches_oracle_and_unsplit(rf, B, Hq, Hkv, Nq, Nk, D, dtype):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tail, n_split = expected_tail_plan(B, Hq, Nq, Nk, sms)
+    assert tail > 0, "the case must exercise the split"
+    nbytes = rf.rf_attn_fwd_workspace_bytes(B, Hq, Nq, Nk, D, False, inputs.DTYPES[dtype])
+    o_bytes = (tail * 256 * n_split * D * 4 + 255) // 256 * 256
+    assert nbytes == o_bytes + tail * 256 * n_split * 4
+    q, k, v = inputs.attn_inputs(B, Hq, Hkv, Nq, Nk, D, dtype, seed=B * 1000 + Nq + Nk)
+    scale = float(np.float32(1 / np.sqrt(D)))
+    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device="cuda")  # stale contents must not matter
+    o_split, lse_split = run_ex(rf, q, k, v, scale, ws)
+    o_whole, lse_whole = run_ex(rf, q, k, v, scale, None)
+    ro, rl = oracle.attention(q, k, v, scale, False)
+    check16(o_split, ro, "split tail")
+    check_lse(lse_split, rl, what="split tail lse")
+    check16(o_whole, ro, "unsplit")
+    # the two schedules differ only in rounding order (fp32 partials merged, then one 16-bit rounding)
+    assert np.abs(to64(o_split) - to64(o_whole)).max() <= 2e-2
+    assert np.abs(to64(lse_split) - to64(lse_whole)).max() <= 1e-3
+
+
+def test_split_tail_rejects_short_workspace(rf):
+    q, k, v = (t.cuda() for t in inputs.attn_inputs(1, 8, 8, 1024, 1024, 64, "f16", seed=5))
+    n = rf.rf_attn_fwd_workspace_bytes(1, 8, 1024, 1024, 64, False, torch.float16)
+    assert n > 0
+    o = torch.empty_like(q)
+    with pytest.raises(rf.RFError, match="workspace"):
+        rf.rf_attn_fwd_ex(q, k, v, o, workspace=torch.empty(n - 16, dtype=torch.uint8, device="cuda"))
+
+
+def test_no_split_cases_need_no_workspace(rf):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert rf.rf_attn_fwd_workspace_bytes(1, sms, 256, 1024, 64, False, torch.float16) == 0  # full last wave
+    assert rf.rf_attn_fwd_workspace_bytes(1, 1, 256, 128, 64, False, torch.float16) == 0  # one key tile
+    assert rf.rf_attn_fwd_workspace_bytes(1, 8, 1024, 1024, 64, True, torch.float16) == 0  # causal
+    assert rf.rf_attn_fwd_workspace_bytes(1, 8, 1024, 1024, 64, False, torch.float32) == 0  # fp32 path
