@@ -469,8 +469,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars->p_ready[t]);
     }
-    if (ok) ok = warp_wait(&bars->o_final[t], 0);
-    if (ok) {
+    // A sliding window can leave query tile 1 of the last unit without any key
+    // tile, when all its rows lie past Nq (every row below Nq sees its own key):
+    // then no PV is issued for it and it has nothing to write.
+    const bool has_keys = jhi > jlo;
+    if (ok && has_keys) ok = warp_wait(&bars->o_final[t], 0);
+    if (ok && has_keys) {
       // epilogue: O / l in the output dtype, LSE in natural log
       tc_fence_after();
       const float inv = 1.0f / l_run;
@@ -512,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (row_ok && lse) lse[static_cast<long long>(bh) * Nq + row] = (m_run + log2f(l_run)) * kLn2;
       }
-    } else {
+    } else if (!ok) {
       if (lane == 0) atomicOr(status, kStatusTimeout);
       bars->abort = 1;
     }

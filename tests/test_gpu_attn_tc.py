@@ -224,3 +224,18 @@ def test_no_split_cases_need_no_workspace(rf):
     assert rf.rf_attn_fwd_workspace_bytes(1, 1, 256, 128, 64, False, torch.float16) == 0  # one key tile
     assert rf.rf_attn_fwd_workspace_bytes(1, 8, 1024, 1024, 64, True, torch.float16) == 0  # causal
     assert rf.rf_attn_fwd_workspace_bytes(1, 8, 1024, 1024, 64, False, torch.float32) == 0  # fp32 path
+
+
+@pytest.mark.parametrize("N,window", [(600, 1), (640, 1), (300, 1), (600, 100), (513, 2)])
+def test_window_with_query_tile_past_the_end(rf, N, window):
+    """The last unit's second query tile lies wholly past N and a narrow window
+    leaves it no key tile: it must finish without waiting for a PV that never
+    comes (the post-test check fails on any recorded wait timeout)."""
+    q, k, v = inputs.attn_inputs(1, 2, 1, N, N, 64, "f16", seed=N + window)
+    scale = float(np.float32(1 / np.sqrt(64)))
+    o, lse = rf.attention(q.cuda(), k.cuda(), v.cuda(), scale=scale, causal=True, window=window)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention(q, k, v, scale, True, window=window)
+    check16(o.cpu(), ro, f"window={window} N={N}")
+    check_lse(lse.cpu(), rl, what="lse")
+    assert rf.rf_device_status(clear=False) == rf.RF_OK
