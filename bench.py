@@ -289,58 +289,66 @@ def oracle_sample(w, host, budget_s=12.0):
         q, k, v = host
         scale = float(np.float32(1.0 / math.sqrt(d["D"])))
         G = d["Hq"] // d["Hkv"]
-        heads = 0
-        for b in range(d["B"]):
-            for h in range(d["Hq"]):
-                if heads and time.perf_counter() - t_start > budget_s:
-                    break
-                # a block of query rows of one head against all its keys
-                rows = min(d["N"], 1024 if d["N"] > 1024 else d["N"])
-                r0 = d["N"] - rows
-                oracle.attention(q[b:b + 1, h:h + 1, r0:], k[b:b + 1, h // G:h // G + 1],
-                                 v[b:b + 1, h // G:h // G + 1], scale, bool(d["causal"]))
-                vis = rows * d["N"] if not d["causal"] else sum(i + 1 for i in range(r0, d["N"]))
-                done_units += 4.0 * vis * d["D"] / 1e12
-                heads += 1
-        what = f"{heads} (batch, head) pairs x the last {rows} query rows against all keys"
+        window = d.get("window", 0)
+        slopes = oracle.alibi_slopes(d["Hq"]) if d.get("alibi") else None
+        rows = min(d["N"], 1024)
+        # blocks of query rows of one (batch, head) against all its keys, cycling
+        # over the whole workload until the time budget is spent
+        blocks = [(b, h, r0) for r0 in range(0, d["N"], rows) for b in range(d["B"]) for h in range(d["Hq"])]
+        n = 0
+        while n == 0 or time.perf_counter() - t_start < budget_s:
+            b, h, r0 = blocks[n % len(blocks)]
+            sel = np.arange(r0, min(r0 + rows, d["N"]))
+            oracle.attention(q[b:b + 1, h:h + 1], k[b:b + 1, h // G:h // G + 1], v[b:b + 1, h // G:h // G + 1],
+                             scale, bool(d["causal"]), rows=sel, window=window,
+                             alibi_slopes=None if slopes is None else slopes[h:h + 1])
+            if not d["causal"]:
+                vis = len(sel) * d["N"]
+            else:
+                vis = int(np.minimum(sel + 1, window if window else d["N"]).sum())
+            done_units += 4.0 * vis * d["D"] / 1e12
+            n += 1
+        what = (f"{n} blocks of up to {rows} query rows x all keys, cycling over the workload's "
+                f"{len(blocks)} (batch, head, row-block) blocks")
     elif w.kind == "decode":
         q, k, v = host
         scale = float(np.float32(1.0 / math.sqrt(d["D"])))
         G = d["Hq"] // d["Hkv"]
-        groups = 0
-        for b in range(d["B"]):
-            for hk in range(d["Hkv"]):
-                if groups and time.perf_counter() - t_start > budget_s:
-                    break
-                oracle.decode(q[b:b + 1, hk * G:(hk + 1) * G], k[b:b + 1, hk:hk + 1], v[b:b + 1, hk:hk + 1], scale)
-                done_units += workmodel.decode_bytes(1, G, 1, d["L"], d["D"], w.dtype) / 1e9
-                groups += 1
-        what = f"{groups} (batch, kv-head) groups of {G} query heads over all {d['L']} keys"
-    elif w.kind == "xent":
-        z, t = host
-        rows = 0
-        while rows < d["rows"] and (rows == 0 or time.perf_counter() - t_start < budget_s):
-            oracle.softmax_xent(z[rows:rows + 64], t[rows:rows + 64])
-            rows += 64
-        done_units = workmodel.xent_bytes(rows, d["vocab"], w.dtype) / 1e9
-        what = f"the first {rows} of {d['rows']} rows"
-    elif w.kind == "rmsnorm":
-        x, r, g = host
-        rows = 0
-        while rows < d["rows"] and (rows == 0 or time.perf_counter() - t_start < budget_s):
-            oracle.rmsnorm(x[rows:rows + 512], r[rows:rows + 512], g, d["eps"])
-            rows += 512
-        done_units = (workmodel.layernorm_bytes(rows, d["cols"], w.dtype, affine=False) + d["cols"] * 2) / 1e9
-        what = f"the first {rows} of {d['rows']} rows"
+        groups = [(b, hk) for b in range(d["B"]) for hk in range(d["Hkv"])]
+        n = 0
+        while n == 0 or time.perf_counter() - t_start < budget_s:
+            b, hk = groups[n % len(groups)]
+            oracle.decode(q[b:b + 1, hk * G:(hk + 1) * G], k[b:b + 1, hk:hk + 1], v[b:b + 1, hk:hk + 1], scale)
+            done_units += workmodel.decode_bytes(1, G, 1, d["L"], d["D"], w.dtype) / 1e9
+            n += 1
+        what = f"{n} (batch, kv-head) groups of {G} query heads over all {d['L']} keys, cycling over {len(groups)}"
     else:
-        x, r, g, b = host
-        rows = 0
-        step = 512
-        while rows < d["rows"] and (rows == 0 or time.perf_counter() - t_start < budget_s):
-            oracle.layernorm(x[rows:rows + step], r[rows:rows + step], g, b, d["eps"])
-            rows += step
-        done_units = workmodel.layernorm_bytes(rows, d["cols"], w.dtype) / 1e9
-        what = f"the first {rows} of {d['rows']} rows"
+        # row blocks of the row-wise cascades, cycling over the workload until the budget is spent
+        step = 64 if w.kind == "xent" else 512
+        n_rows = d["rows"]
+        n = 0
+        rows_done = 0
+        while n == 0 or time.perf_counter() - t_start < budget_s:
+            r0 = (n * step) % n_rows
+            r1 = min(r0 + step, n_rows)
+            if w.kind == "xent":
+                z, t = host
+                oracle.softmax_xent(z[r0:r1], t[r0:r1])
+            elif w.kind == "rmsnorm":
+                x, r, g = host
+                oracle.rmsnorm(x[r0:r1], r[r0:r1], g, d["eps"])
+            else:
+                x, r, g, b = host
+                oracle.layernorm(x[r0:r1], r[r0:r1], g, b, d["eps"])
+            rows_done += r1 - r0
+            n += 1
+        if w.kind == "xent":
+            done_units = workmodel.xent_bytes(rows_done, d["vocab"], w.dtype) / 1e9
+        elif w.kind == "rmsnorm":
+            done_units = (workmodel.layernorm_bytes(rows_done, d["cols"], w.dtype, affine=False) + d["cols"] * 2) / 1e9
+        else:
+            done_units = workmodel.layernorm_bytes(rows_done, d["cols"], w.dtype) / 1e9
+        what = f"{rows_done} rows in blocks of {step}, cycling over the workload's {n_rows} rows"
     secs = time.perf_counter() - t_start
     return done_units / secs, what, secs
 
