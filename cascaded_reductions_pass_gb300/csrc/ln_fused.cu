@@ -3,19 +3,25 @@
 // section 1 traffic example and section 2 Pattern 2: mean -> variance ->
 // normalise; section 4 places eps inside the square root).
 //
-// The cascade mean -> M2 -> normalise runs in the incremental form of
-// RedFuser (Figure 4): each thread keeps a running (count, mean, M2) that it
-// updates as each 16-byte block of the row arrives (Chan, Golub and LeVeque's
-// pairwise combine: the M2 of the union is M2_a + M2_b + delta^2 n_a n_b / n,
-// the additive correction of level 2 when level 1 moves).  The same combine
-// merges the threads of a row through warp shuffles and then across warps in
-// shared memory.  The row stays in registers between the statistics and the
-// normalisation, so x and the residual are read from HBM once and y is
-// written once.
+// The cascade mean -> M2 -> normalise runs fused in one pass, in the
+// incremental form of RedFuser (Figure 4): level 2's dependence on level 1 is
+// the additive correction M2 = sum((h - K)^2) - n (mean - K)^2 for any shift
+// K, so with one shift K for the whole row (its first element h_0, which every
+// thread of the row reads) both levels are plain running sums,
+// S1 = sum(h - K) and S2 = sum((h - K)^2), updated as each element arrives and
+// merged across lanes (shuffles) and warps (shared memory) with combine op +;
+// then mean = K + S1/n and M2 = S2 - S1^2/n once per row.  The shift keeps
+// that subtraction free of cancellation: K is a sample of the same row, so
+// S1/n is of the order of the row's spread, not of its mean.  (A per-thread
+// shift would need Chan, Golub and LeVeque's pairwise combine of
+// (n, mean, M2) at every merge step; a common shift turns it into two sums,
+// and the per-row merge was this kernel's serial latency.)  The row stays in
+// registers between the statistics and the normalisation, so x and the
+// residual are read from HBM once and y is written once.
 //
 // The kernel is bound by instruction issue as much as by HBM, so the
-// element-wise work runs on packed fp32 pairs (fma/add/mul .f32x2) and the
-// in-thread combine uses compile-time reciprocals.  The affine map keeps the
+// element-wise work runs on packed fp32 pairs (fma/add/mul .f32x2): three
+// packed operations per pair for the statistics.  The affine map keeps the
 // centred form y = (h - mean) * (gamma * rstd) + beta, so a constant row gives
 // exactly beta.
 //
@@ -26,20 +32,6 @@
 
 namespace rf {
 namespace {
-
-struct Stats {
-  float n, mean, m2;
-};
-
-// General pairwise combine (counts may differ or be zero).
-__device__ __forceinline__ Stats chan(Stats a, Stats b) {
-  if (b.n == 0.f) return a;
-  if (a.n == 0.f) return b;
-  const float n = a.n + b.n;
-  const float f = __fdividef(b.n, n);
-  const float d = b.mean - a.mean;
-  return Stats{n, fmaf(d, f, a.mean), a.m2 + b.m2 + d * d * a.n * f};
-}
 
 // 16-byte vector <-> packed fp32 pairs.
 template <Dt DT>
@@ -116,8 +108,7 @@ __global__ void __launch_bounds__(1024) ln_fused_kernel(const uint4* __restrict_
                                                         float inv_cols, float eps) {
   using V = Vec2<DT>;
   constexpr int P = V::P;
-  constexpr int E = 2 * P;  // elements per 16-byte vector
-  __shared__ Stats s_warp[32];
+  __shared__ float2 s_warp[32];
 
   const int rows_per_cta = blockDim.x / tpr;
   const int slot = threadIdx.x / tpr;
@@ -139,66 +130,69 @@ __global__ void __launch_bounds__(1024) ln_fused_kernel(const uint4* __restrict_
     }
   }
 
-  // Levels 1-2, incremental: fold each 16-byte block into the running stats.
-  // Valid blocks of a thread form a prefix (i < count), so block i joins a
-  // running count of E*i and the combine factor n_b/n is the constant 1/(i+1).
+  // Levels 1-2, incremental: running sums about the row's first element K
+  // (valid blocks form a prefix i < count; blocks past the row end are skipped).
+  float shift = 0.f;
+  if (row_ok) {
+    uint64_t x0[P], r0[P];
+    V::unpack(__ldg(x + base), x0);
+    if (r) {
+      V::unpack(__ldg(r + base), r0);
+    } else {
+      r0[0] = 0;
+    }
+    float unused;
+    f2unpack(add_f32x2(x0[0], r0[0]), shift, unused);
+  }
+  const uint64_t negk2 = f2pack(-shift, -shift);
   uint64_t h[VPT][P];
-  Stats st{0.f, 0.f, 0.f};
+  uint64_t s1 = 0, s2 = 0;  // packed pairs: two partial sums each
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     uint64_t xp[P], rp[P];
     V::unpack(xv[i], xp);
     V::unpack(rv[i], rp);
-    uint64_t s2 = 0;
+    const bool valid = t + i * tpr < nvec;
 #pragma unroll
     for (int k = 0; k < P; ++k) {
       h[i][k] = add_f32x2(xp[k], rp[k]);
-      s2 = k == 0 ? h[i][0] : add_f32x2(s2, h[i][k]);
-    }
-    const float mb = hsum(s2) * (1.0f / E);
-    const uint64_t negmb = f2pack(-mb, -mb);
-    uint64_t q2 = 0;
-#pragma unroll
-    for (int k = 0; k < P; ++k) {
-      const uint64_t d = add_f32x2(h[i][k], negmb);
-      q2 = k == 0 ? mul_f32x2(d, d) : fma_f32x2(d, d, q2);
-    }
-    const float q = hsum(q2);
-    if (t + i * tpr < nvec) {
-      if (i == 0) {
-        st = Stats{float(E), mb, q};
-      } else {
-        constexpr float kE = float(E);
-        const float f = 1.0f / float(i + 1);  // folded at compile time (unrolled i)
-        const float d = mb - st.mean;
-        st.mean = fmaf(d, f, st.mean);
-        st.m2 = st.m2 + q + d * d * (kE * i) * f;
-        st.n += kE;
+      if (valid) {
+        const uint64_t d = add_f32x2(h[i][k], negk2);
+        s1 = add_f32x2(s1, d);
+        s2 = fma_f32x2(d, d, s2);
       }
     }
   }
-  // Merge the threads of the warp (all 32 lanes belong to this row).
+  float a1 = hsum(s1), a2 = hsum(s2);
+  // Merge the threads of the warp (all 32 lanes belong to this row): combine op +.
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    Stats b{__shfl_xor_sync(0xffffffffu, st.n, o), __shfl_xor_sync(0xffffffffu, st.mean, o),
-            __shfl_xor_sync(0xffffffffu, st.m2, o)};
-    st = chan(st, b);
+    a1 += __shfl_xor_sync(0xffffffffu, a1, o);
+    a2 += __shfl_xor_sync(0xffffffffu, a2, o);
   }
   // Merge the warps of the row through shared memory (same order in every thread).
   const int warps_per_row = tpr >> 5;
   if (warps_per_row > 1) {
     const int w = threadIdx.x >> 5;
-    if ((threadIdx.x & 31) == 0) s_warp[w] = st;
+    if ((threadIdx.x & 31) == 0) s_warp[w] = make_float2(a1, a2);
     __syncthreads();
     const int w0 = slot * warps_per_row;
-    st = s_warp[w0];
-    for (int j = 1; j < warps_per_row; ++j) st = chan(st, s_warp[w0 + j]);
+    float2 acc = s_warp[w0];
+    for (int j = 1; j < warps_per_row; ++j) {
+      acc.x += s_warp[w0 + j].x;
+      acc.y += s_warp[w0 + j].y;
+    }
+    a1 = acc.x;
+    a2 = acc.y;
   }
+  const float mean_k = a1 * inv_cols;  // mean - K
+  const float mean = shift + mean_k;
+  const float var = fmaxf(fmaf(-mean_k, mean_k, a2 * inv_cols), 0.f);
   if (!row_ok) return;
 
   // Level 3: y = (h - mean) * (gamma * rstd) + beta, three packed ops per pair.
-  const float rstd = rsqrtf(st.m2 * inv_cols + eps);
-  const uint64_t rstd2 = f2pack(rstd, rstd), negmean2 = f2pack(-st.mean, -st.mean);
+  const float rstd = rsqrtf(var + eps);
+  const uint64_t rstd2 = f2pack(rstd, rstd), negmean2 = f2pack(-mean, -mean);
   const uint64_t one2 = f2pack(1.f, 1.f), zero2 = 0;
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
@@ -310,7 +304,7 @@ cudaError_t launch_dt(const void* x, const void* r, const void* g, const void* b
                       int rows, int cols, float eps, cudaStream_t s) {
   constexpr int E = 2 * Vec2<DT>::P;
   const int nvec = cols / E;
-  const int vpt = nvec >= 256 ? 4 : (nvec >= 64 ? 2 : 1);
+  const int vpt = nvec >= 128 ? 4 : (nvec >= 64 ? 2 : 1);  // one warp per row from 128 vectors up
   int tpr = (nvec + vpt - 1) / vpt;
   tpr = (tpr + 31) & ~31;
   const int rows_per_cta = tpr >= 256 ? 1 : 256 / tpr;
