@@ -28,6 +28,9 @@ incremental form that the CUDA kernels use:
   ("Operator Fusion" guide, section 3, fusible patterns: RMSNorm).
 * ``softmax_xent``  -- row max -> sum exp -> cross-entropy loss, its LSE and
   gradient ("Operator Fusion" guide, section 3: softmax + cross-entropy).
+* ``rope``          -- rotary position embedding of Q and K rows, the
+  pre-matmul transformation of AttnFuse (Abstract; Figure 1), rotate-half
+  pairing.
 
 Every function is pinned by the CPU tests (brute force on tiny inputs, closed
 forms, invariants, a library second opinion); no function is "parity unpinned".
@@ -40,6 +43,7 @@ from .reference import (  # noqa: F401
     layernorm,
     lse_merge,
     rmsnorm,
+    rope,
     softmax_xent,
     split_bounds,
 )

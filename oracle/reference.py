@@ -226,3 +226,30 @@ def alibi_slopes(n_heads):
     2^(-8 (h+1) / H) for h = 0..H-1.  The pages name ALiBi (AttnFuse, Table 6)
     without its slopes; this is the usual choice."""
     return np.array([2.0 ** (-8.0 * (h + 1) / n_heads) for h in range(n_heads)])
+
+
+def rope(x, positions, base=10000.0):
+    """Rotary position embedding of the rows of x.
+
+    AttnFuse names RoPE as the pre-matmul transformation of Q and K used by
+    every major LLM (Abstract; Figure 1) but prints no formula.  Reading (the
+    usual definition, in the rotate-half pairing of the Llama models the page
+    names): for head dimension D and i < D/2, the pair (x_i, x_{i+D/2}) of a
+    row at position p is turned by the angle p * base^(-2i/D):
+        y_i       = x_i cos(theta) - x_{i+D/2} sin(theta)
+        y_{i+D/2} = x_i sin(theta) + x_{i+D/2} cos(theta)
+
+    Shapes: x [..., N, D] with D even; positions [N] (integers).  Returns y as
+    float64 with the shape of x.
+    """
+    x = _f64(x)
+    D = x.shape[-1]
+    if D % 2:
+        raise ValueError("rope needs an even head dimension")
+    half = D // 2
+    pos = np.asarray(positions, dtype=np.float64).reshape(-1, 1)          # [N, 1]
+    inv_freq = float(base) ** (-2.0 * np.arange(half, dtype=np.float64) / D)  # [D/2]
+    theta = pos * inv_freq[None, :]                                         # [N, D/2]
+    c, s = np.cos(theta), np.sin(theta)
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * c - x2 * s, x1 * s + x2 * c], axis=-1)

@@ -36,6 +36,10 @@ MUTANTS = {
     "xent_lse_missing_max": ("lse = (m + np.log(l))[..., 0]", "lse = (np.log(l))[..., 0]"),
     "xent_grad_no_onehot": ("t[valid]] -= 1.0", "t[valid]] -= 0.0"),
     "rms_residual_dropped": ("    h = x + r\n    n = h.shape[-1]\n    ms", "    h = x + 0 * r\n    n = h.shape[-1]\n    ms"),
+    "rope_sin_sign": ("[x1 * c - x2 * s, x1 * s + x2 * c]", "[x1 * c + x2 * s, -x1 * s + x2 * c]"),
+    "rope_interleaved_pairs": ("x1, x2 = x[..., :half], x[..., half:]", "x1, x2 = x[..., 0::2], x[..., 1::2]"),
+    "rope_frequency_exponent": ("** (-2.0 * np.arange(half, dtype=np.float64) / D)",
+                                "** (-1.0 * np.arange(half, dtype=np.float64) / D)"),
 }
 
 
@@ -49,5 +53,5 @@ def apply(name):
         raise RuntimeError(f"mutant {name}: snippet found {src.count(old)} times")
     code = compile(src.replace(old, new), ref.__file__, "exec")
     exec(code, ref.__dict__)
-    for fn in ("attention", "decode", "decode_partials", "layernorm", "lse_merge", "split_bounds", "rmsnorm", "softmax_xent", "alibi_slopes"):
+    for fn in ("attention", "decode", "decode_partials", "layernorm", "lse_merge", "split_bounds", "rmsnorm", "softmax_xent", "alibi_slopes", "rope"):
         setattr(oracle, fn, getattr(ref, fn))

@@ -17,7 +17,8 @@ import _oracle_mutants  # noqa: E402
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 PINS = ["tests/test_oracle_attention.py", "tests/test_oracle_merge.py",
-        "tests/test_oracle_layernorm.py", "tests/test_oracle_xent.py", "tests/test_golden.py"]
+        "tests/test_oracle_layernorm.py", "tests/test_oracle_xent.py", "tests/test_oracle_rope.py",
+        "tests/test_golden.py"]
 
 
 @pytest.mark.parametrize("name", sorted(_oracle_mutants.MUTANTS))
