@@ -7,11 +7,14 @@ input, inputs already resident in HBM.  The default workload is the
 non-causal fp16 attention forward (B=4 H=12 N=4096 D=64, seed 1); the line's
 ``parts`` object reports the other workloads (causal GQA bf16 attention,
 split-KV decode, residual+LayerNorm and RMSNorm, softmax cross-entropy, the
-sliding-window and ALiBi attention variants, tiny fp32 attention) measured the
+sliding-window and ALiBi attention variants, rotary embedding of Q and K, tiny
+fp32 attention) measured the
 same way in the same run, and ``ablations`` times the fusion-level and
-non-incremental variants of the LayerNorm and cross-entropy cascades.  Each timed step is bracketed by CUDA events on the
-launching stream, with an L2 flush (a 512 MiB memset, larger than the 129 MB
-L2) before every step, outside the events.  Under torchrun each rank runs an
+non-incremental variants of the LayerNorm and cross-entropy cascades.  Each
+timed step is bracketed by CUDA events on the launching stream, with an L2
+flush before every step, outside the events: a 512 MiB memset (larger than
+the 129 MB L2), then a 256 MiB read so that no dirty flush line is left for
+the timed kernel to write back.  Under torchrun each rank runs an
 independent replica (no data-path collective: the work of one call does not
 shard across GPUs here), ``value`` is the units all ranks processed divided by
 the slowest rank's time.
@@ -159,6 +162,12 @@ class Runner:
             self.metric, self.unit, self.bound = "split-KV decode GB/s", "GB/s", "hbm"
             self.units = self.bytes / 1e9
             self.kernel_file, self.kernel = "decode_split.cu", "decode_split (+ lse_merge)"
+        elif self.w.kind == "rope":
+            self.bytes = workmodel.rope_bytes(d["B"], d["Hq"], d["Hkv"], d["N"], d["D"], self.dtype)
+            self.flops = 6.0 * d["B"] * (d["Hq"] + d["Hkv"]) * d["N"] * d["D"] / 2
+            self.metric, self.unit, self.bound = "rotary embedding GB/s", "GB/s", "hbm"
+            self.units = self.bytes / 1e9
+            self.kernel_file, self.kernel = "rope.cu", "rope"
         elif self.w.kind == "xent":
             self.bytes = workmodel.xent_bytes(d["rows"], d["vocab"], self.dtype)
             self.flops = 4.0 * d["rows"] * d["vocab"]
@@ -192,6 +201,10 @@ class Runner:
             if not d["causal"] and self.dtype != "f32":
                 self.ws = self.rf.attn_workspace(q, self.dev_in[1], False)
             self.launches = 2 if self.ws is not None else 1
+        elif self.w.kind == "rope":
+            self.o = torch.empty_like(self.dev_in[0])
+            self.ko = torch.empty_like(self.dev_in[1])
+            self.outs = [self.o, self.ko]
         elif self.w.kind == "xent":
             self.o = torch.empty(d["rows"], dtype=torch.float32, device=dev)
             self.lse = torch.empty(d["rows"], dtype=torch.float32, device=dev)
@@ -220,6 +233,8 @@ class Runner:
                                       scale=self.scale)
         elif self.w.kind == "rmsnorm":
             rf.rf_rmsnorm_fused(ins[0], ins[1], ins[2], self.o, eps=d["eps"])
+        elif self.w.kind == "rope":
+            rf.rf_rope_qk(ins[0], ins[1], self.o, self.ko, base=d["base"])
         elif self.w.kind == "xent":
             rf.rf_softmax_xent(ins[0], ins[1], self.o, self.lse)
         else:
@@ -228,6 +243,22 @@ class Runner:
     def describe(self):
         d = dict(self.w.dims)
         return {"workload": self.w.name, **d, "dtype": self.dtype, "seed": self.w.seed}
+
+
+class L2Flush:
+    """Leaves L2 cold and clean before a timed step: a 512 MiB memset (larger
+    than the 129 MB L2) evicts every line of the step's inputs, then a 256 MiB
+    read replaces the memset's dirty lines with clean ones.  Without the read,
+    the next kernel pays the write-back of up to 129 MB of the flush buffer
+    (measured: 5-9 us on an HBM-bound launch of 100-400 MB)."""
+
+    def __init__(self, dev):
+        self.write = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.read = torch.zeros(L2_FLUSH_BYTES // 8, dtype=torch.float32, device=dev)
+
+    def zero_(self):
+        self.write.zero_()
+        self.read.sum()  # one read-only reduction: no temporary, nothing written back
 
 
 def time_steps(runner, steps, warmup, flush):
@@ -322,6 +353,17 @@ def oracle_sample(w, host, budget_s=12.0):
             done_units += workmodel.decode_bytes(1, G, 1, d["L"], d["D"], w.dtype) / 1e9
             n += 1
         what = f"{n} (batch, kv-head) groups of {G} query heads over all {d['L']} keys, cycling over {len(groups)}"
+    elif w.kind == "rope":
+        q, k = host
+        pos = np.arange(d["N"])
+        planes = [(t, b, h) for t in (0, 1) for b in range(d["B"]) for h in range(d["Hq"] if t == 0 else d["Hkv"])]
+        n = 0
+        while n == 0 or time.perf_counter() - t_start < budget_s:
+            t, b, h = planes[n % len(planes)]
+            oracle.rope((q if t == 0 else k)[b, h], pos, d["base"])
+            done_units += 2 * d["N"] * d["D"] * (2 if w.dtype != "f32" else 4) / 1e9
+            n += 1
+        what = f"{n} (tensor, batch, head) planes of {d['N']} rows, cycling over {len(planes)}"
     else:
         # row blocks of the row-wise cascades, cycling over the workload until the budget is spent
         step = 64 if w.kind == "xent" else 512
@@ -484,7 +526,7 @@ def main():
             if i >= args.warmup:
                 per_step.append((v, secs))
         val = float(np.mean([v for v, _ in per_step]))
-        unit = "TFLOP/s" if w.kind == "attn" else "GB/s"  # decode, layernorm, rmsnorm: GB/s
+        unit = "TFLOP/s" if w.kind == "attn" else "GB/s"  # decode, layernorm, rmsnorm, xent, rope: GB/s
         ms = float(np.mean([s for _, s in per_step]) * 1e3)
         print(json.dumps({
             "impl": "reference", "metric": "fused cascaded-reduction throughput (CPU fp64 oracle)", "value": val,
@@ -505,7 +547,7 @@ def main():
     dev = torch.device("cuda", local)
     rf.load()
     peaks = load_peaks()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     sampler = ClockSampler(local)
     sampler.start()
 
@@ -561,7 +603,9 @@ def main():
             "metric": runner.metric, "value": value, "unit": runner.unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": runner.dtype, "data": "synthetic",
-            "config": {**runner.describe(), "l2": "flushed before every step (512 MiB memset, outside the events)",
+            "config": {**runner.describe(),
+                       "l2": "flushed before every step, outside the events: 512 MiB memset, then a 256 MiB read "
+                             "so that L2 holds only clean lines",
                        "parallelism": f"replicas{world}" if world > 1 else "single-gpu"},
             "roofline": res["roofline"],
             "e2e": e2e,

@@ -52,6 +52,7 @@ _SIGNATURES = {
     "rf_device_status": ([_vp, _i], _i),
     "rf_selftest_wait_timeout": ([ctypes.c_uint, _vp], _i),
     "rf_ablation_workspace_bytes": ([_i, _i, _i, _i, _i], _sz),
+    "rf_rope_qk": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp], _i),
     "rf_layernorm_ablation": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _f, _i, _vp, _sz, _i, _vp], _i),
     "rf_softmax_xent_ablation": ([_vp, _vp, _vp, _vp, _i, _i, ctypes.c_longlong, _i, _vp, _sz, _i, _vp], _i),
 }
@@ -363,6 +364,25 @@ def layernorm(x, residual, gamma, beta, eps=1e-5, want_residual_out=False, strea
     return (out, rout) if want_residual_out else out
 
 
+def rf_rope_qk(q, k=None, q_out=None, k_out=None, base=10000.0, pos_offset=0, stream=None):
+    """Rotary embedding of q [B,Hq,N,D] (and k [B,Hkv,N,D]) at positions pos_offset + n; in place by default."""
+    q_out = q if q_out is None else q_out
+    k_out = k if k_out is None else k_out
+    B, Hq, N, D = q.shape
+    Hkv = 0
+    if k is not None:
+        if k.dim() != 4 or k.shape[0] != B or k.shape[2] != N or k.shape[3] != D or k.dtype != q.dtype:
+            raise ValueError("k must be [B,Hkv,N,D] of q's dtype")
+        Hkv = k.shape[1]
+        if tuple(k_out.shape) != tuple(k.shape) or k_out.dtype != k.dtype:
+            raise ValueError("k_out must match k")
+    if tuple(q_out.shape) != tuple(q.shape) or q_out.dtype != q.dtype:
+        raise ValueError("q_out must match q")
+    _check(load().rf_rope_qk(_dev(q, "q"), _dev(k, "k", True), _dev(q_out, "q_out"), _dev(k_out, "k_out", True),
+                             B, Hq, Hkv, N, D, float(base), int(pos_offset), _code(q.dtype), _stream(stream)))
+    return q_out, k_out
+
+
 LN_VARIANTS = {0: "fused incremental", 1: "fused non-incremental (row in shared memory)",
                2: "reductions fused, normalise separate", 3: "unfused"}
 XENT_VARIANTS = {0: "fused incremental", 1: "fused two-pass", 2: "unfused"}
@@ -420,6 +440,6 @@ __all__ = [
     "rf_lse_merge", "rf_layernorm_fused", "rf_rmsnorm_fused", "rmsnorm", "rf_softmax_xent", "softmax_xent",
     "attention", "decode", "decode_workspace", "decode_partials_view", "layernorm",
     "rf_ablation_workspace_bytes", "rf_layernorm_ablation", "rf_softmax_xent_ablation", "ablation_workspace",
-    "LN_VARIANTS", "XENT_VARIANTS",
+    "LN_VARIANTS", "XENT_VARIANTS", "rf_rope_qk",
     "RF_OK", "RF_ERR_INVALID_ARG", "RF_ERR_UNSUPPORTED", "RF_ERR_CUDA", "RF_ERR_TIMEOUT",
 ]

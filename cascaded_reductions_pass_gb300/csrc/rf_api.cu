@@ -382,6 +382,37 @@ rf_status_t rf_layernorm_fused(const void* x, const void* residual, const void* 
                   "rf_layernorm_fused");
 }
 
+rf_status_t rf_rope_qk(const void* q, const void* k, void* q_out, void* k_out, int B, int Hq, int Hkv, int N, int D,
+                       float base, int pos_offset, rf_dtype_t dtype, void* stream) {
+  if (!q || !q_out) return fail(RF_ERR_INVALID_ARG, "rf_rope_qk: q and q_out must be non-null");
+  if ((k == nullptr) != (k_out == nullptr))
+    return fail(RF_ERR_INVALID_ARG, "rf_rope_qk: k and k_out must both be given or both be null");
+  if (B <= 0 || Hq <= 0 || N <= 0 || D <= 0 || (k && Hkv <= 0))
+    return fail(RF_ERR_INVALID_ARG, "rf_rope_qk: sizes must be positive (B=%d Hq=%d Hkv=%d N=%d D=%d)", B, Hq, Hkv,
+                N, D);
+  if (!(base > 0.0f) || !std::isfinite(base) || base == 1.0f)
+    return fail(RF_ERR_INVALID_ARG, "rf_rope_qk: base must be finite, positive and not 1");
+  if (pos_offset < 0) return fail(RF_ERR_INVALID_ARG, "rf_rope_qk: pos_offset must be >= 0");
+  if (!valid_dtype(dtype)) return fail(RF_ERR_INVALID_ARG, "rf_rope_qk: unknown dtype %d", int(dtype));
+  if (!aligned16(q) || !aligned16(k) || !aligned16(q_out) || !aligned16(k_out))
+    return fail(RF_ERR_INVALID_ARG, "rf_rope_qk: pointers must be 16-byte aligned");
+  if (dtype == RF_F32) return fail(RF_ERR_UNSUPPORTED, "rf_rope_qk: fp32 is not supported (f16, bf16)");
+  if (D != 64 && D != 128 && D != 256) return fail(RF_ERR_UNSUPPORTED, "rf_rope_qk: D=%d (64, 128, 256)", D);
+  if (static_cast<long long>(pos_offset) + N > (1LL << 24))
+    return fail(RF_ERR_UNSUPPORTED, "rf_rope_qk: positions reach %lld, past 2^24",
+                static_cast<long long>(pos_offset) + N);
+  // one CTA indexes (B*Hq + B*Hkv) rows x 8 positions x D/16 chunk pairs in 32 bits (with headroom)
+  if ((static_cast<long long>(B) * Hq + static_cast<long long>(B) * Hkv) * 8 * (D / 16) > 0x7fff0000LL)
+    return fail(RF_ERR_UNSUPPORTED, "rf_rope_qk: B*(Hq+Hkv) too large");
+  RF_TRY(check_dev_ptr(q, "q"));
+  RF_TRY(check_dev_ptr(k, "k"));
+  RF_TRY(check_dev_ptr(q_out, "q_out"));
+  RF_TRY(check_dev_ptr(k_out, "k_out"));
+  return launched(rf::launch_rope_qk(q, k, q_out, k_out, B * Hq, k ? B * Hkv : 0, N, D, static_cast<double>(base),
+                                     pos_offset, static_cast<rf::Dt>(dtype), static_cast<cudaStream_t>(stream)),
+                  "rf_rope_qk");
+}
+
 rf_status_t rf_selftest_wait_timeout(unsigned timeout_us, void* stream) {
   if (timeout_us == 0 || timeout_us > 1000000u)
     return fail(RF_ERR_INVALID_ARG, "rf_selftest_wait_timeout: timeout_us must be in [1, 1000000]");

@@ -65,6 +65,12 @@ cudaError_t launch_ln_ablation(const void* x, const void* r, const void* g, cons
 cudaError_t launch_xent_ablation(const void* logits, const long long* targets, float* loss, float* lse, int rows,
                                  int vocab, long long ignore, int variant, void* ws, Dt dt, cudaStream_t s);
 
+// rotary position embedding of Q and K rows, one HBM pass (rope.cu); 16-bit,
+// D in {64, 128, 256}; q_out / k_out may alias q / k
+constexpr int kRopeMaxHalf = 128;
+cudaError_t launch_rope_qk(const void* q, const void* k, void* q_out, void* k_out, int BHq, int BHkv, int N, int D,
+                           double base, int pos_offset, Dt dt, cudaStream_t s);
+
 // TMA descriptor encoding through the driver entry point (rf_api.cu).
 // 3-D tensor [outer][rows][inner] of 16-bit elements, box {64, box_rows, 1},
 // 128-byte swizzle; returns false (and sets *err) on failure.

@@ -126,6 +126,9 @@ WORKLOADS = {
                                    dict(B=4, Hq=12, Hkv=12, N=4096, D=64, causal=1, window=256)),
     "attn_causal_alibi_f16_d64": Workload("attn_causal_alibi_f16_d64", "attn", "f16", 9,
                                           dict(B=4, Hq=12, Hkv=12, N=4096, D=64, causal=1, alibi=1)),
+    # rotary embedding of Q and K at AttnFuse's RoPE + causal shape (Tables 4-5)
+    "rope_qk_f16_d64": Workload("rope_qk_f16_d64", "rope", "f16", 10,
+                                dict(B=4, Hq=12, Hkv=12, N=4096, D=64, base=10000.0)),
 }
 
 
@@ -145,4 +148,7 @@ def make(workload: Workload):
         return x, r, g
     if workload.kind == "xent":
         return xent_inputs(d["rows"], d["vocab"], workload.dtype, workload.seed)
+    if workload.kind == "rope":
+        q, k, _ = attn_inputs(d["B"], d["Hq"], d["Hkv"], d["N"], d["N"], d["D"], workload.dtype, workload.seed)
+        return q, k
     raise ValueError(workload.kind)

@@ -87,3 +87,9 @@ def ablation_bytes(op, variant, rows, cols, dtype):
         small = rows * 8 + rows * 8  # int64 targets; fp32 loss and lse
         return {0: T, 1: 2 * T, 2: 2 * T + rows * 16}[variant] + small
     raise ValueError(op)
+
+
+def rope_bytes(B, Hq, Hkv, N, D, dtype):
+    """Q and K read once and written once (out of place or in place alike)."""
+    e = ELEM_BYTES[dtype]
+    return 2 * B * (Hq + Hkv) * N * D * e

@@ -297,6 +297,30 @@ rf_status_t rf_rmsnorm_fused(const void* x, const void* residual, const void* ga
 rf_status_t rf_softmax_xent(const void* logits, const long long* targets, float* loss, float* lse, void* grad,
                             int rows, int vocab, long long ignore_index, rf_dtype_t dtype, void* stream);
 
+/*
+ * rf_rope_qk -- rotary position embedding of Q and K, the pre-matmul
+ * transformation of AttnFuse (Abstract; Figure 1), as one HBM pass ahead of
+ * the attention call.  For i < D/2 the pair (x_i, x_{i+D/2}) of the row at
+ * position p = pos_offset + n turns by theta = p * base^(-2i/D):
+ *   y_i = x_i cos theta - x_{i+D/2} sin theta,
+ *   y_{i+D/2} = x_i sin theta + x_{i+D/2} cos theta  (rotate-half pairing).
+ *
+ *   q      [B, Hq, N, D]  dtype (read)        q_out  [B, Hq, N, D]  (written)
+ *   k      [B, Hkv, N, D] dtype (read)        k_out  [B, Hkv, N, D] (written)
+ * k and k_out are both null (rotate Q only) or both non-null.  An output may
+ * be its own input (in place).  Angles are formed to about 1e-7 rad for any
+ * position below 2^24.
+ *
+ * Supported: dtype RF_F16 / RF_BF16; D in {64, 128, 256}; base > 0, finite,
+ * not 1; pos_offset >= 0 and pos_offset + N <= 2^24; pointers 16-byte aligned.
+ * Errors: RF_ERR_INVALID_ARG for null q/q_out, a k without k_out (or the
+ * reverse), non-positive sizes, a bad base or offset, misalignment;
+ * RF_ERR_UNSUPPORTED for other D or dtypes and positions past 2^24;
+ * RF_ERR_CUDA if the launch fails.
+ */
+rf_status_t rf_rope_qk(const void* q, const void* k, void* q_out, void* k_out, int B, int Hq, int Hkv, int N, int D,
+                       float base, int pos_offset, rf_dtype_t dtype, void* stream);
+
 /* Message for the last non-OK status returned on this host thread ("" if none). */
 const char* rf_last_error(void);
 

@@ -248,3 +248,24 @@ def test_attn_ex_rejects_misaligned_workspace(lib):
     opts = AttnOpts(0, 0, None, 0x10008, 1 << 20)
     st = lib.rf_attn_fwd_ex(P, P, P, P, None, 1, 2, 1, 8, 8, 64, 0.125, ctypes.byref(opts), 1, S)
     assert st == rf.RF_ERR_INVALID_ARG and "aligned" in lib.rf_last_error().decode()
+
+
+@pytest.mark.parametrize("kw, status, msg", [
+    (dict(q=None), rf.RF_ERR_INVALID_ARG, "non-null"),
+    (dict(k_out=None), rf.RF_ERR_INVALID_ARG, "both"),
+    (dict(N=0), rf.RF_ERR_INVALID_ARG, "positive"),
+    (dict(base=1.0), rf.RF_ERR_INVALID_ARG, "base"),
+    (dict(base=-2.0), rf.RF_ERR_INVALID_ARG, "base"),
+    (dict(pos_offset=-1), rf.RF_ERR_INVALID_ARG, "pos_offset"),
+    (dict(q=MIS), rf.RF_ERR_INVALID_ARG, "aligned"),
+    (dict(dtype=0), rf.RF_ERR_UNSUPPORTED, "fp32"),
+    (dict(D=96), rf.RF_ERR_UNSUPPORTED, "D=96"),
+    (dict(pos_offset=(1 << 24) - 4), rf.RF_ERR_UNSUPPORTED, "2^24"),
+])
+def test_rope_rejects(lib, kw, status, msg):
+    a = dict(q=P, k=P, q_out=P, k_out=P, B=1, Hq=2, Hkv=1, N=8, D=64, base=10000.0, pos_offset=0, dtype=1)
+    a.update(kw)
+    st = lib.rf_rope_qk(a["q"], a["k"], a["q_out"], a["k_out"], a["B"], a["Hq"], a["Hkv"], a["N"], a["D"],
+                        a["base"], a["pos_offset"], a["dtype"], S)
+    assert st == status
+    assert msg in lib.rf_last_error().decode()
