@@ -450,6 +450,7 @@ def measure(name, dev, steps, warmup, flush, peaks, with_e2e=True, batch=None):
         achieved, peak = r.flops / (ms / 1e3) / 1e12, 152 * 128 * 2 * 2.07e9 / 1e12
     res = {
         "workload": name, "value": val, "unit": r.unit, "ms_per_step": ms,
+        "ms_median": float(np.median(times)),
         "ms_p10": float(np.percentile(times, 10)), "ms_p90": float(np.percentile(times, 90)),
         "roofline": {"bound": r.bound, "achieved": achieved, "peak": peak, "unit": achieved_unit,
                      "frac": achieved / peak, "traffic": kernel_traffic(r.kernel_file, name),
@@ -642,7 +643,7 @@ def main():
             "e2e": e2e,
             "gpu_launches": launches, "clocks": clocks, "cpu_baseline": cpu,
             "device_status": int(status), "parts": parts, "ablations": ablations,
-            "ms_p10": res["ms_p10"], "ms_p90": res["ms_p90"],
+            "ms_median": res["ms_median"], "ms_p10": res["ms_p10"], "ms_p90": res["ms_p90"],
         }
         print(json.dumps(line))
     if world > 1:

@@ -128,6 +128,52 @@ def test_welford_chan_incremental_form_reaches_plain_result():
     np.testing.assert_allclose(yy, y[0], atol=1e-12)
 
 
+def test_shifted_sums_reach_plain_result():
+    """The one-pass form with one shift K for the whole row (its first element):
+    S1 = sum(h - K), S2 = sum((h - K)^2) accumulate as plain running sums in any
+    partition and order, and mean = K + S1/n, M2 = S2 - S1^2/n is the plain
+    two-pass statistics exactly (in fp64, to rounding)."""
+    x = _rand((1, 101), 18) * 4 + 10
+    y, h = oracle.layernorm(x, np.zeros_like(x), np.ones(101), np.zeros(101), 1e-5)
+    row = h[0]
+    k = row[0]
+    parts = [(float(np.sum(row[i:i + 13] - k)), float(np.sum((row[i:i + 13] - k) ** 2))) for i in range(0, 101, 13)]
+    s1 = math.fsum(p[0] for p in parts)
+    s2 = math.fsum(p[1] for p in parts)
+    n = row.size
+    mean, m2 = k + s1 / n, s2 - s1 * s1 / n
+    np.testing.assert_allclose(mean, row.mean(), rtol=1e-14)
+    np.testing.assert_allclose(m2 / n, np.mean((row - row.mean()) ** 2), rtol=1e-12)
+    yy = (row - mean) / math.sqrt(m2 / n + 1e-5)
+    np.testing.assert_allclose(yy, y[0], atol=1e-12)
+
+
+def test_shifted_sums_keep_float32_variance_for_a_large_mean():
+    """Why the shift: in float32, the unshifted one-pass formula
+    E[h^2] - E[h]^2 cancels catastrophically for a row of mean 1000 and spread
+    0.5; sums about the row's first element keep the variance accurate."""
+    rng = np.random.default_rng(19)
+    row = (1000.0 + 0.5 * rng.standard_normal(4096)).astype(np.float32)
+    exact = np.var(row.astype(np.float64))
+    n = np.float32(row.size)
+    s1 = np.float32(0)
+    s2 = np.float32(0)
+    k = row[0]
+    for v in row:  # float32 running sums, element by element
+        d = np.float32(v - k)
+        s1 = np.float32(s1 + d)
+        s2 = np.float32(s2 + d * d)
+    var_shifted = np.float32(s2 / n - (s1 / n) * (s1 / n))
+    t1 = np.float32(0)
+    t2 = np.float32(0)
+    for v in row:
+        t1 = np.float32(t1 + v)
+        t2 = np.float32(t2 + v * v)
+    var_naive = np.float32(t2 / n - (t1 / n) * (t1 / n))
+    assert abs(var_shifted - exact) / exact < 1e-3
+    assert abs(var_naive - exact) / exact > 1e-2  # the form the shift avoids
+
+
 # ---------------------------------------------------------------- RMSNorm
 def brute_rms(x, r, g, eps):
     y = np.zeros_like(x)
