@@ -288,8 +288,9 @@ rf_status_t rf_rmsnorm_fused(const void* x, const void* residual, const void* ga
  *
  * Supported: dtype RF_F32 / RF_F16 / RF_BF16; vocab a multiple of 16 bytes'
  * worth of elements (8 for 16-bit, 4 for fp32); logits and grad 16-byte
- * aligned.  One CTA per row: sized for rows in the thousands (training
- * batches); any rows >= 1 is correct.
+ * aligned.  Many rows run one CTA per row; fewer rows than multiprocessors
+ * run each row on a thread-block cluster of up to 8 CTAs that merge their
+ * partial (max, sum exp) through distributed shared memory.  Any rows >= 1.
  * Errors: RF_ERR_INVALID_ARG for null logits/targets/loss, non-positive sizes,
  * misalignment or a vocab that is not a whole number of vectors; RF_ERR_CUDA
  * if the launch fails.

@@ -60,3 +60,30 @@ def test_xent_full_size_sampled(rf):
     rloss, rlse, _ = oracle.softmax_xent(logits[rows], targets[rows])
     assert np.abs(to64(lse)[rows] - rlse).max() <= 1e-3
     assert np.abs(to64(loss)[rows] - rloss).max() <= 1e-3
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("rows,V", [(1, 128256), (2, 50000), (16, 128256), (64, 50000), (151, 32768), (152, 32768),
+                                    (3, 16392)])
+def test_xent_few_rows_cluster_path(rf, dtype, rows, V):
+    """Few rows: each row is split over a cluster of up to 8 CTAs whose partial
+    (max, sum exp) meet in distributed shared memory (ragged slices included)."""
+    logits, targets = inputs.xent_inputs(rows, V, dtype, seed=rows * 7 + V)
+    targets[::5] = -100
+    bad = rows > 2  # row 1 gets a target outside [0, V): NaN loss, LSE still defined
+    if bad:
+        targets[1] = V + 3
+    loss, lse, grad = run(rf, logits, targets)
+    valid_t = targets.clone()
+    if bad:
+        valid_t[1] = -100  # the oracle takes targets in range or ignored only
+    rloss, rlse, rgrad = oracle.softmax_xent(logits, valid_t)
+    tol = 1e-5 * max(1.0, float(np.abs(rlse).max())) if dtype == "f32" else 1e-3
+    assert np.abs(to64(lse) - rlse).max() <= tol
+    keep = np.ones(rows, dtype=bool)
+    if bad:
+        keep[1] = False
+        assert np.isnan(to64(loss)[1])
+    assert np.abs(to64(loss)[keep] - rloss[keep]).max() <= tol
+    assert (to64(grad)[::5] == 0).all()
+    assert np.abs(to64(grad)[keep] - rgrad[keep]).max() <= (1e-5 if dtype == "f32" else 2e-2)
