@@ -396,11 +396,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kBN; ++c)
           if (key0 + c >= lim || key0 + c < first) s[c] = __float_as_uint(-INFINITY);
       }
-      if constexpr (ALIBI) {  // s <- s * scale * log2 e + slope * log2 e * (key - row)
+      if constexpr (ALIBI) {
+        // s <- s * scale * log2 e + slope * log2 e * (key - row), one packed FMA per
+        // pair: the bias of the pair (2e, 2e+1) rides in one of four packed
+        // accumulators that advance by 8 * slope per pair of their own.
         const float base = slope2 * static_cast<float>(key0 - row);
+        uint64_t bias[4];
 #pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          s[c] = __float_as_uint(fmaf(__uint_as_float(s[c]), sl2, fmaf(slope2, static_cast<float>(c), base)));
+        for (int k = 0; k < 4; ++k)
+          bias[k] = f2pack(fmaf(slope2, static_cast<float>(2 * k), base),
+                           fmaf(slope2, static_cast<float>(2 * k + 1), base));
+        const uint64_t step = f2pack(8.f * slope2, 8.f * slope2);
+#pragma unroll
+        for (int e = 0; e < kBN / 2; ++e) {
+          const uint64_t r = fma_f32x2(u2pack(s[2 * e], s[2 * e + 1]), sl2x2, bias[e & 3]);
+          f2unpack_u(r, s[2 * e], s[2 * e + 1]);
+          bias[e & 3] = add_f32x2(bias[e & 3], step);
+        }
       }
       // level 1: tile max over the row, four independent 3-input max chains
       float mx4[4];
