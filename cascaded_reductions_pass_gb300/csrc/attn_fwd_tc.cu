@@ -7,9 +7,11 @@
 // level 1 (reduce max, combine +) keeps a running row max m; levels 2 and 3
 // (reduce +, combine *) keep the running sum l and the running output O, both
 // corrected by exp(m_old - m_new) when m rises.  The correction is applied
-// lazily: m moves only when a tile's max exceeds it by more than 2^8 (in
-// base 2), which stays exact because l and O are built against the same m, and
-// keeps P <= 256.
+// lazily, which stays exact because l and O are always built against the same
+// m: m moves only when a tile's max exceeds it by more than 2^8 (in base 2),
+// which keeps P <= 256.  Non-causal D = 64 rows speculate: once m is finite, P
+// is formed against it without scanning the tile, and m moves only when a half
+// row's sum of P exceeds 2^15, so P stays <= 2^15.
 //
 // CTA = two query tiles of 128 rows (rows r0..r0+255 of one (batch, head)),
 // 12 warps:
@@ -66,6 +68,10 @@ constexpr int kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // base-2 units
+// Speculative P (rows with a finite running max): every P of a half row stays
+// <= 2^kSpecLog2, far inside fp16's range, or the half is redone.
+constexpr float kSpecLog2 = 15.0f;
+constexpr float kSpecMax = 32768.0f;  // 2^kSpecLog2
 constexpr int kRegsCtl = 80;       // per thread, warps 0-3 after reallocation
 constexpr int kRegsSoftmax = 208;  // per thread, warps 4-11 after reallocation
 
@@ -113,6 +119,64 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, unsigned parity) {
   return __all_sync(0xffffffffu, ok);
 }
 
+// Max of the scores s[C0, kBN) of a row, in the base-2 units of the exponent
+// (ALiBi rows already hold scaled scores): independent 3-input max chains of
+// 32 elements each.
+template <int C0, bool ALIBI>
+__device__ __forceinline__ float scaled_max_from(const uint32_t* s, float sl2) {
+  constexpr int kChains = (kBN - C0) / 32;
+  float mx[kChains];
+#pragma unroll
+  for (int q4 = 0; q4 < kChains; ++q4) {
+    const uint32_t* sq = s + C0 + 32 * q4;
+    float m = max3f(__uint_as_float(sq[0]), __uint_as_float(sq[1]), __uint_as_float(sq[2]));
+#pragma unroll
+    for (int i = 3; i + 1 < 32; i += 2) m = max3f(m, __uint_as_float(sq[i]), __uint_as_float(sq[i + 1]));
+    mx[q4] = fmaxf(m, __uint_as_float(sq[31]));
+  }
+  float m = mx[0];
+#pragma unroll
+  for (int q4 = 1; q4 < kChains; ++q4) m = fmaxf(m, mx[q4]);
+  return ALIBI ? m : m * sl2;
+}
+
+// P = 2^(s * sl2 - m) for the pairs [E0, E1) of a row (16-bit, packed into
+// pk), and their sum, kept in four packed accumulators.
+template <Dt DT, bool ALIBI, int E0, int E1>
+__device__ __forceinline__ float exp_pairs(const uint32_t* s, uint64_t sl2x2, uint64_t negm2, uint32_t* pk) {
+  uint64_t sum2[4];
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) sum2[q4] = f2pack(0.f, 0.f);
+#pragma unroll
+  for (int e = E0; e < E1; ++e) {
+    const uint64_t x = ALIBI ? add_f32x2(u2pack(s[2 * e], s[2 * e + 1]), negm2)
+                             : fma_f32x2(u2pack(s[2 * e], s[2 * e + 1]), sl2x2, negm2);
+    float x0, x1;
+    f2unpack(x, x0, x1);
+    const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
+    sum2[e & 3] = add_f32x2(sum2[e & 3], f2pack(p0, p1));
+    pk[e] = Pack<DT>::pack2(p0, p1);
+  }
+  float lo, hi;
+  f2unpack(add_f32x2(add_f32x2(sum2[0], sum2[1]), add_f32x2(sum2[2], sum2[3])), lo, hi);
+  return lo + hi;
+}
+
+// A packed pair of 16-bit P values times a.
+template <Dt DT>
+__device__ __forceinline__ uint32_t scale_pair(uint32_t w, float a) {
+  float lo, hi;
+  if constexpr (DT == Dt::BF16) {
+    lo = bf16lo(w);
+    hi = bf16hi(w);
+  } else {
+    const float2 f = unpack_f16x2(w);
+    lo = f.x;
+    hi = f.y;
+  }
+  return Pack<DT>::pack2(lo * a, hi * a);
+}
+
 // MASK: 0 none, 1 causal (top-left), 2 causal with a sliding window of
 // `window` keys (key j visible to query i iff i - window < j <= i).
 // ALIBI: add slope_h * (j - i) to each scaled score (slopes per query head).
@@ -124,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const float* __restrict__ alibi, unsigned* status, int n_full, int n_split,
                    float* __restrict__ o_part, float* __restrict__ lse_part) {
   constexpr bool CAUSAL = MASK >= 1;
+  constexpr bool kSpec = D == 64 && MASK == 0 && !ALIBI;
   using C = Cfg<D>;
   constexpr int S = C::kStages;
   constexpr bool kBF16 = DT == Dt::BF16;
@@ -374,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t sl2x2 = f2pack(sl2, sl2);
     const float slope2 = ALIBI ? __ldg(alibi + (bh % Hq)) * kLog2e : 0.f;
     float m_run = -INFINITY, l_run = 0.f;
+    bool spec = kSpec;  // warp-uniform: cleared by the first failed speculation
     bool ok = true;
     for (int j = jlo; j < jhi; ++j) {
       const int jt = j - jlo;  // this tile's own key-tile count: barrier phases
@@ -414,40 +480,63 @@ __global__ void __launch_bounds__(kThreads, 1)
           bias[e & 3] = add_f32x2(bias[e & 3], step);
         }
       }
-      // level 1: tile max over the row, four independent 3-input max chains
-      float mx4[4];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const uint32_t* sq = s + 32 * q4;
-        float m = max3f(__uint_as_float(sq[0]), __uint_as_float(sq[1]), __uint_as_float(sq[2]));
-#pragma unroll
-        for (int i = 3; i + 1 < 32; i += 2) m = max3f(m, __uint_as_float(sq[i]), __uint_as_float(sq[i + 1]));
-        mx4[q4] = fmaxf(m, __uint_as_float(sq[31]));
-      }
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      const float mt = ALIBI ? mx : mx * sl2;
-      const bool need = mt > m_run + kRescaleThreshold;
-      const float m_new = need ? mt : m_run;
-      // a row can see no key of this tile (sliding window): keep it at zero weight
-      const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = ex2_ftz(m_run - m_use);
-      // level 2: P = 2^(s*sl2 - m) (16-bit, packed in registers), running sum in
-      // four packed accumulators; all exponentials run before any wait below
-      const uint64_t negm2 = f2pack(-m_use, -m_use);
-      uint64_t sum2[4];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) sum2[q4] = f2pack(0.f, 0.f);
       uint32_t pk[kBN / 2];
+      float m_new = m_run, tsum = 0.f;
+      bool need = false;
+      // Speculation (non-causal D = 64 without ALiBi): a row whose running max m
+      // is finite first forms P against m without scanning the tile, which is
+      // exact as long as no P exceeds kSpecMax; the sum of each half row bounds
+      // that.  When a first half fails, the row is redone from the tile max;
+      // when only a second half fails, that half is rescanned alone.  After one
+      // failure the warp stops speculating (steadily rising scores would make
+      // it fail on every tile).
+      if constexpr (kSpec) {
+        bool exact = !spec || __any_sync(0xffffffffu, m_run == -INFINITY);
+        float h0, h1;
+        for (;;) {
+          if (exact) {
+            const float mt = scaled_max_from<0, ALIBI>(s, sl2);
+            m_new = mt > m_run + kRescaleThreshold ? mt : m_run;
+          }
+          const float m_use = m_new == -INFINITY ? 0.f : m_new;
+          const uint64_t negm2 = f2pack(-m_use, -m_use);
+          h0 = exp_pairs<DT, ALIBI, 0, kBN / 4>(s, sl2x2, negm2, pk);
+          if (exact) {
+            h1 = exp_pairs<DT, ALIBI, kBN / 4, kBN / 2>(s, sl2x2, negm2, pk);
+            break;
+          }
+          if (!__any_sync(0xffffffffu, !(h0 <= kSpecMax))) {
+            h1 = exp_pairs<DT, ALIBI, kBN / 4, kBN / 2>(s, sl2x2, negm2, pk);
+            const bool big = !(h1 <= kSpecMax);
+            if (__any_sync(0xffffffffu, big)) {
+              // every first-half P is <= 2^kSpecLog2, so m + kSpecLog2 bounds that half
+              spec = false;
+              const float mt = scaled_max_from<kBN / 2, ALIBI>(s, sl2);
+              m_new = big ? fmaxf(mt, m_run + kSpecLog2) : m_run;
+              const float a = ex2_ftz(m_run - m_new);
 #pragma unroll
-      for (int e = 0; e < kBN / 2; ++e) {
-        const uint64_t x = ALIBI ? add_f32x2(u2pack(s[2 * e], s[2 * e + 1]), negm2)
-                                 : fma_f32x2(u2pack(s[2 * e], s[2 * e + 1]), sl2x2, negm2);
-        float x0, x1;
-        f2unpack(x, x0, x1);
-        const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
-        sum2[e & 3] = add_f32x2(sum2[e & 3], f2pack(p0, p1));
-        pk[e] = Pack<DT>::pack2(p0, p1);
+              for (int e = 0; e < kBN / 4; ++e) pk[e] = scale_pair<DT>(pk[e], a);
+              h0 *= a;
+              h1 = exp_pairs<DT, ALIBI, kBN / 4, kBN / 2>(s, sl2x2, f2pack(-m_new, -m_new), pk);
+            }
+            break;
+          }
+          exact = true;  // a first half failed: redo the row from the tile max
+          spec = false;
+        }
+        need = m_new != m_run && m_new != -INFINITY;
+        tsum = h0 + h1;
+      } else {
+        // level 1: the tile max over the row decides m; level 2: P = 2^(s*sl2 - m)
+        const float mt = scaled_max_from<0, ALIBI>(s, sl2);
+        need = mt > m_run + kRescaleThreshold;
+        m_new = need ? mt : m_run;
+        // a row can see no key of this tile (sliding window): keep it at zero weight
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        tsum = exp_pairs<DT, ALIBI, 0, kBN / 2>(s, sl2x2, f2pack(-m_use, -m_use), pk);
       }
+      // all exponentials run before any wait below
+      const float alpha = need ? ex2_ftz(m_run - m_new) : 1.f;
       if constexpr (C::kSepP) {  // PV_t(j-1) must be done before P_t and O_t are touched
         if (jt > 0) {
           if (!(ok = warp_wait(&bars->pv_done[t], (jt - 1) & 1))) break;
@@ -456,10 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int cc = 0; cc < kBN / 16; ++cc) tc_st8(tP + 8 * cc, pk + 8 * cc);
-      const uint64_t sumv = add_f32x2(add_f32x2(sum2[0], sum2[1]), add_f32x2(sum2[2], sum2[3]));
-      float sum_lo, sum_hi;
-      f2unpack(sumv, sum_lo, sum_hi);
-      l_run = fmaf(l_run, alpha, sum_lo + sum_hi);
+      l_run = fmaf(l_run, alpha, tsum);
       // level 3 correction: rescale O in TMEM when some row's max moved
       if (jt > 0 && __any_sync(0xffffffffu, need)) {
         const uint64_t a2 = f2pack(alpha, alpha);

@@ -84,6 +84,46 @@ def test_one_hot_dominant_key(rf):
     check16(o[0, 0], to64(v[0, 0, targets]), "one-hot")
 
 
+# Scores that climb from key tile to key tile, so that a row's running max is
+# overtaken in every way the kernel handles it: on the row's first tile, in the
+# first half (keys 0-63) of a later tile, in its second half only, and not at
+# all.  Levels are natural-log units per half tile of 64 keys; a jump of 14 is
+# 2^20 in P.  In the first pattern the running max is first overtaken in a
+# second half, in the second pattern in a first half.
+RISING_LEVELS = {"second_half_first": [[0, 0], [0, 14], [30, 30], [31, 29], [5, 60]],
+                 "first_half_first": [[0, 0], [1, 0], [20, 20], [20, 21], [40, 40]]}
+
+
+@pytest.mark.parametrize("D,dtype,causal,window,alibi,levels", [
+    (64, "f16", False, 0, False, "second_half_first"),
+    (64, "bf16", False, 0, False, "first_half_first"),
+    (64, "bf16", True, 0, False, "second_half_first"),
+    (128, "f16", True, 0, False, "first_half_first"),
+    (128, "bf16", False, 0, False, "second_half_first"),
+    (64, "f16", True, 300, True, "second_half_first"),
+])
+def test_rising_scores_take_every_rescale_path(rf, D, dtype, causal, window, alibi, levels):
+    pattern = RISING_LEVELS[levels]
+    N, H = 128 * len(pattern), 2
+    rng = np.random.default_rng(D + window)
+    u = rng.standard_normal(D)
+    u /= np.linalg.norm(u)
+    level = np.repeat(np.asarray(pattern, dtype=np.float64).reshape(-1), 64)
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    q = (np.sqrt(D) * u + 0.05 * rng.standard_normal((1, H, N, D)))
+    k = level[:, None] * u + 0.3 * rng.standard_normal((1, H, N, D))
+    v = rng.standard_normal((1, H, N, D))
+    q, k, v = (torch.from_numpy(x).to(tdt) for x in (q, k, v))
+    scale = float(np.float32(1 / np.sqrt(D)))
+    slopes = oracle.alibi_slopes(H) if alibi else None
+    o, lse = rf.attention(q.cuda(), k.cuda(), v.cuda(), scale=scale, causal=causal, window=window,
+                          alibi_slopes=torch.tensor(slopes, dtype=torch.float32).cuda() if alibi else None)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention(q, k, v, scale, causal, window=window, alibi_slopes=slopes)
+    check16(o.cpu(), ro, f"rising scores D={D} causal={causal} W={window}")
+    check_lse(lse.cpu(), rl, what="rising scores lse")
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["attn_fwd_f16_d64", "attn_fwd_causal_gqa_bf16_d128"])
 def test_full_size_sampled(rf, name):
