@@ -153,6 +153,8 @@ class Runner:
             self.units = self.flops / 1e12
             self.kernel_file = "attn_fwd_f32.cu" if self.dtype == "f32" else "attn_fwd_tc.cu"
             self.kernel = "attn_fwd_f32" if self.dtype == "f32" else "attn_fwd_tc"
+            if self.dtype != "f32" and d["D"] == 64 and 0 < self.window <= 1024:  # the persistent windowed kernel
+                self.kernel_file, self.kernel = "attn_fwd_tc_window.cu", "attn_fwd_tc_window"
             if self.dtype == "f32":
                 self.bound = "alu"
         elif self.w.kind == "decode":

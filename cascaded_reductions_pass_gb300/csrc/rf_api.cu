@@ -234,6 +234,9 @@ rf_status_t attn_impl(const char* name, const void* q, const void* k, const void
     if (ws_bytes < need)
       return fail(RF_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", name, need, ws_bytes);
     RF_TRY(check_dev_ptr(ws, "workspace"));
+  } else if (dtype != RF_F32 && causal && window > 0 && window <= rf::kWindowPersistMax && D == 64) {
+    // the persistent windowed kernel
+    sms = rf::device_sm_count();
   }
   if (dtype == RF_F32)
     return launched(rf::launch_attn_f32(static_cast<const float*>(q), static_cast<const float*>(k),

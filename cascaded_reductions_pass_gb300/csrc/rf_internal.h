@@ -50,6 +50,15 @@ cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* o,
                            int window, const float* alibi, Dt dt, unsigned* status, void* ws, int sms,
                            cudaStream_t s);
 
+// causal sliding-window attention at D = 64 for 16-bit inputs as a persistent
+// kernel, one CTA per SM walking a list of 256-row units (attn_fwd_tc_window.cu);
+// with sms <= 0, one CTA per unit.  launch_attn_tc sends windows of up to
+// kWindowPersistMax keys there.
+constexpr int kWindowPersistMax = 1024;
+cudaError_t launch_attn_tc_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                                  int Hkv, int Nq, int Nk, float scale, int window, const float* alibi, Dt dt,
+                                  unsigned* status, int sms, cudaStream_t s);
+
 // multiprocessor count of the current device (cached per device; 0 on error)
 int device_sm_count();
 

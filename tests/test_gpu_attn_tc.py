@@ -154,6 +154,8 @@ def test_full_size_sampled(rf, name):
     (1, 2, 640, 128, 0, True, "bf16"),
     (1, 3, 1100, 64, 300, True, "f16"),     # window and ALiBi together
     (1, 2, 256, 128, 5000, False, "bf16"),  # window wider than the sequence = causal
+    (1, 2, 2600, 64, 1500, False, "f16"),   # a wide window at D = 64: one CTA per unit
+    (1, 2, 1300, 64, 1024, True, "bf16"),   # the widest window the persistent kernel takes
 ])
 def test_variants(rf, B, H, N, D, window, alibi, dtype):
     q, k, v = inputs.attn_inputs(B, H, H, N, N, D, dtype, seed=N + window)
@@ -264,6 +266,32 @@ def test_no_split_cases_need_no_workspace(rf):
     assert rf.rf_attn_fwd_workspace_bytes(1, 1, 256, 128, 64, False, torch.float16) == 0  # one key tile
     assert rf.rf_attn_fwd_workspace_bytes(1, 8, 1024, 1024, 64, True, torch.float16) == 0  # causal
     assert rf.rf_attn_fwd_workspace_bytes(1, 8, 1024, 1024, 64, False, torch.float32) == 0  # fp32 path
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,window,alibi,dtype", [
+    (3, 32, 8, 1300, 200, False, "f16"),   # GQA, ragged last unit
+    (2, 40, 40, 850, 1, True, "bf16"),     # the last unit's second query tile sees no key tile
+    (8, 48, 48, 512, 64, False, "f16"),    # about five units per CTA
+])
+def test_window_units_walked_by_persistent_ctas(rf, B, Hq, Hkv, N, window, alibi, dtype):
+    """D = 64 sliding windows run one CTA per SM over a list of units, so these
+    shapes (several units per CTA) cross every item boundary of the schedule:
+    Q buffers, K/V ring slots and barrier phases carried from unit to unit."""
+    q, k, v = inputs.attn_inputs(B, Hq, Hkv, N, N, 64, dtype, seed=N + window + Hq)
+    scale = float(np.float32(1 / np.sqrt(64)))
+    slopes = oracle.alibi_slopes(Hq) if alibi else None
+    o, lse = rf.attention(q.cuda(), k.cuda(), v.cuda(), scale=scale, causal=True, window=window,
+                          alibi_slopes=torch.tensor(slopes, dtype=torch.float32).cuda() if alibi else None)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([[0, 127, 128, 255, 256, N - 1], np.random.default_rng(N).integers(0, N, 40)]))
+    G = Hq // Hkv
+    for b, h in [(0, 0), (B // 2, Hq // 2 + 1), (B - 1, Hq - 1)]:
+        ro, rl = oracle.attention(q[b:b + 1, h:h + 1], k[b:b + 1, h // G:h // G + 1], v[b:b + 1, h // G:h // G + 1],
+                                  scale, True, rows=rows, window=window,
+                                  alibi_slopes=slopes[h:h + 1] if alibi else None)
+        check16(o[b:b + 1, h:h + 1, rows].cpu(), ro, f"persistent window b={b} h={h}")
+        check_lse(lse[b:b + 1, h:h + 1, rows].cpu(), rl, what="persistent window lse")
+    assert np.isfinite(to64(o.cpu())).all()
 
 
 @pytest.mark.parametrize("N,window", [(600, 1), (640, 1), (300, 1), (600, 100), (513, 2)])
