@@ -357,7 +357,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tP = tmem + lane_off + (C::kSepP ? C::kPCol + t * (kBN / 2) : t * kBN);
     const uint32_t tO = tmem + lane_off + C::kOCol + t * D;
     const int jlo = t == 0 ? lo0 : lo1, jhi = t == 0 ? nt0 : nt1;
-    const int tile_row0 = r0 + t * kBM;
     const uint64_t sl2x2 = f2pack(sl2, sl2);
     const float slope2 = ALIBI ? __ldg(alibi + (bh % Hq)) * kLog2e : 0.f;
     float m_run = -INFINITY, l_run = 0.f;
@@ -376,10 +375,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bars->s_free[t]);
       }
       const int key0 = j * kBN;
-      if (key0 + kBN > Nk || (CAUSAL && key0 + kBN - 1 > tile_row0) ||
-          (MASK == 2 && key0 < tile_row0 + kBM - window)) {
-        const int lim = CAUSAL ? min(Nk, row + 1) : Nk;   // keys below lim ...
-        const int first = MASK == 2 ? row - window + 1 : 0;  // ... and from first on are visible
+      if constexpr (CAUSAL) {
+        // columns below cl and from cf on are visible; each bound costs one
+        // compare per column only where some row of the warp needs it
+        const int cl = min(Nk, row + 1) - key0;
+        if (__any_sync(0xffffffffu, cl < kBN)) {
+#pragma unroll
+          for (int c = 0; c < kBN; ++c)
+            if (c >= cl) s[c] = __float_as_uint(-INFINITY);
+        }
+        if constexpr (MASK == 2) {
+          const int cf = row - window + 1 - key0;
+          if (__any_sync(0xffffffffu, cf > 0)) {
+#pragma unroll
+            for (int c = 0; c < kBN; ++c)
+              if (c < cf) s[c] = __float_as_uint(-INFINITY);
+          }
+        }
+      } else if (key0 + kBN > Nk) {
+        const int lim = Nk, first = 0;  // keys below lim and from first on are visible
 #pragma unroll
         for (int c = 0; c < kBN; ++c)
           if (key0 + c >= lim || key0 + c < first) s[c] = __float_as_uint(-INFINITY);

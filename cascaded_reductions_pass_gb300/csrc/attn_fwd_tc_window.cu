@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int nfin = 0;  // items whose O this query tile has finished
     bool ok = true;
     for (int k = 0; ok && k < kMaxItems; ++k) {
-      int row, jlo, jhi, tile_row0, bh;
+      int row, jlo, jhi, bh;
       {
         const WinItem it = items[k];
         if (it.bh < 0 || aborted(bars)) break;
@@ -346,7 +346,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         row = it.r0 + t * kBM + qw * 32 + lane;
         jlo = t == 0 ? it.lo0 : it.lo1;
         jhi = t == 0 ? it.nt0 : it.nt1;
-        tile_row0 = it.r0 + t * kBM;
       }
       const float slope2 = ALIBI ? __ldg(alibi + (bh % Hq)) * kLog2e : 0.f;
       float m_run = -INFINITY, l_run = 0.f;
@@ -361,12 +360,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();  // S_t may be overwritten by the next S_t now
         mbar_arrive(&bars->s_free[t]);
         const int key0 = j * kBN;
-        if (key0 + kBN > sc.Nk || key0 + kBN - 1 > tile_row0 || key0 < tile_row0 + kBM - sc.window) {
-          const int lim = min(sc.Nk, row + 1);    // keys below lim ...
-          const int first = row - sc.window + 1;  // ... and from first on are visible
+        // columns below cl and from cf on are visible; a tile is cut by at most
+        // the diagonal (or Nk) from above and the window's edge from below, and
+        // each bound costs one compare per column only where some row needs it
+        const int cl = min(sc.Nk, row + 1) - key0;
+        const int cf = row - sc.window + 1 - key0;
+        if (__any_sync(0xffffffffu, cl < kBN)) {
 #pragma unroll
           for (int c = 0; c < kBN; ++c)
-            if (key0 + c >= lim || key0 + c < first) s[c] = __float_as_uint(-INFINITY);
+            if (c >= cl) s[c] = __float_as_uint(-INFINITY);
+        }
+        if (__any_sync(0xffffffffu, cf > 0)) {
+#pragma unroll
+          for (int c = 0; c < kBN; ++c)
+            if (c < cf) s[c] = __float_as_uint(-INFINITY);
         }
         if constexpr (ALIBI) {
           // s <- s * scale * log2 e + slope * log2 e * (key - row), one packed FMA per
