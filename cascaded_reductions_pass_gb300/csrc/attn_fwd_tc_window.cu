@@ -43,7 +43,7 @@ constexpr int kWStages = 3;                  // K/V ring depth
 constexpr int kWTiles = 2 * 2 * kWQBytes + 2 * kWStages * kWKVBytes;  // Q [tile][buffer], K ring, V ring
 constexpr int kWOCol = 2 * kBN;              // O0 at 256, O1 at 320
 constexpr int kWPCol = 2 * kBN + 2 * kWD;    // P0 at 384, P1 at 448
-constexpr int kMaxItems = 256;               // items per CTA (the grid widens beyond that)
+constexpr int kMaxItems = 1024;              // items per CTA (the grid widens beyond that)
 
 struct alignas(8) WinBars {
   uint64_t q_full[2][2], q_empty[2][2];  // [query tile][Q buffer]

@@ -294,6 +294,27 @@ def test_window_units_walked_by_persistent_ctas(rf, B, Hq, Hkv, N, window, alibi
     assert np.isfinite(to64(o.cpu())).all()
 
 
+@pytest.mark.slow
+def test_window_grid_widens_past_the_unit_list(rf):
+    """A CTA's unit list holds 1024 units, so with more than 1024 units per SM the
+    windowed kernel launches more CTAs than SMs: here 163,840 units of 256 rows
+    (5.4 GB per tensor)."""
+    B, H, N, window = 64, 64, 10240, 128
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert B * H * (N // 256) > 1024 * sms
+    g = torch.Generator(device="cuda").manual_seed(11)
+    q, k, v = (torch.randn(B, H, N, 64, device="cuda", generator=g, dtype=torch.float16) for _ in range(3))
+    o, lse = rf.attention(q, k, v, scale=0.125, causal=True, window=window)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([[0, 255, 256, N - 1], np.random.default_rng(5).integers(0, N, 24)]))
+    for b, h in [(0, 0), (B // 2, 17), (B - 1, H - 1)]:
+        ro, rl = oracle.attention(q[b:b + 1, h:h + 1].cpu(), k[b:b + 1, h:h + 1].cpu(), v[b:b + 1, h:h + 1].cpu(),
+                                  0.125, True, rows=rows, window=window)
+        check16(o[b:b + 1, h:h + 1, rows].cpu(), ro, f"widened grid b={b} h={h}")
+        check_lse(lse[b:b + 1, h:h + 1, rows].cpu(), rl, what="widened grid lse")
+    del q, k, v, o, lse
+
+
 @pytest.mark.parametrize("N,window", [(600, 1), (640, 1), (300, 1), (600, 100), (513, 2)])
 def test_window_with_query_tile_past_the_end(rf, N, window):
     """The last unit's second query tile lies wholly past N and a narrow window

@@ -17,7 +17,7 @@ import random
 import pytest
 
 S = 3          # K/V ring stages
-MAX_ITEMS = 256
+MAX_ITEMS = 1024
 
 
 def cta_items(BH, nqt, Nk, window, G, b):
