@@ -124,6 +124,22 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- workloads
+# metric, unit and bound per workload kind; both arms report the same metric and unit
+METRICS = {
+    "attn": ("attention forward TFLOP/s", "TFLOP/s", "tensor"),
+    "decode": ("split-KV decode GB/s", "GB/s", "hbm"),
+    "rope": ("rotary embedding GB/s", "GB/s", "hbm"),
+    "xent": ("softmax cross-entropy GB/s", "GB/s", "hbm"),
+    "rmsnorm": ("residual+RMSNorm GB/s", "GB/s", "hbm"),
+    "layernorm": ("residual+LayerNorm GB/s", "GB/s", "hbm"),
+}
+
+
+def workload_config(w):
+    """The workload part of the bench line's config, the same for both arms."""
+    return {"workload": w.name, **w.dims, "dtype": w.dtype, "seed": w.seed}
+
+
 class Runner:
     """One workload: its inputs on the device, one step of the hot path, its work."""
 
@@ -149,7 +165,7 @@ class Runner:
             if d.get("alibi"):
                 self.alibi = rf.alibi_slopes(d["Hq"], device=dev)
             self.bytes = workmodel.attn_bytes(d["B"], d["Hq"], d["Hkv"], d["N"], d["N"], d["D"], self.dtype)
-            self.metric, self.unit, self.bound = "attention forward TFLOP/s", "TFLOP/s", "tensor"
+            self.metric, self.unit, self.bound = METRICS["attn"]
             self.units = self.flops / 1e12
             self.kernel_file = "attn_fwd_f32.cu" if self.dtype == "f32" else "attn_fwd_tc.cu"
             self.kernel = "attn_fwd_f32" if self.dtype == "f32" else "attn_fwd_tc"
@@ -161,31 +177,31 @@ class Runner:
             self.scale = float(np.float32(1.0 / math.sqrt(d["D"])))
             self.bytes = workmodel.decode_bytes(d["B"], d["Hq"], d["Hkv"], d["L"], d["D"], self.dtype)
             self.flops = workmodel.decode_flops(d["B"], d["Hq"], d["L"], d["D"])
-            self.metric, self.unit, self.bound = "split-KV decode GB/s", "GB/s", "hbm"
+            self.metric, self.unit, self.bound = METRICS["decode"]
             self.units = self.bytes / 1e9
             self.kernel_file, self.kernel = "decode_split.cu", "decode_split (+ lse_merge)"
         elif self.w.kind == "rope":
             self.bytes = workmodel.rope_bytes(d["B"], d["Hq"], d["Hkv"], d["N"], d["D"], self.dtype)
             self.flops = 6.0 * d["B"] * (d["Hq"] + d["Hkv"]) * d["N"] * d["D"] / 2
-            self.metric, self.unit, self.bound = "rotary embedding GB/s", "GB/s", "hbm"
+            self.metric, self.unit, self.bound = METRICS["rope"]
             self.units = self.bytes / 1e9
             self.kernel_file, self.kernel = "rope.cu", "rope"
         elif self.w.kind == "xent":
             self.bytes = workmodel.xent_bytes(d["rows"], d["vocab"], self.dtype)
             self.flops = 4.0 * d["rows"] * d["vocab"]
-            self.metric, self.unit, self.bound = "softmax cross-entropy GB/s", "GB/s", "hbm"
+            self.metric, self.unit, self.bound = METRICS["xent"]
             self.units = self.bytes / 1e9
             self.kernel_file, self.kernel = "xent_fused.cu", "xent"
         elif self.w.kind == "rmsnorm":
             self.bytes = workmodel.layernorm_bytes(d["rows"], d["cols"], self.dtype, affine=False) + d["cols"] * 2
             self.flops = 4.0 * d["rows"] * d["cols"]
-            self.metric, self.unit, self.bound = "residual+RMSNorm GB/s", "GB/s", "hbm"
+            self.metric, self.unit, self.bound = METRICS["rmsnorm"]
             self.units = self.bytes / 1e9
             self.kernel_file, self.kernel = "ln_fused.cu", "rms_fused"
         else:
             self.bytes = workmodel.layernorm_bytes(d["rows"], d["cols"], self.dtype)
             self.flops = 10.0 * d["rows"] * d["cols"]
-            self.metric, self.unit, self.bound = "residual+LayerNorm GB/s", "GB/s", "hbm"
+            self.metric, self.unit, self.bound = METRICS["layernorm"]
             self.units = self.bytes / 1e9
             self.kernel_file, self.kernel = "ln_fused.cu", "ln_fused"
         self.dev_in = [t.to(dev) for t in self.host]
@@ -243,8 +259,7 @@ class Runner:
             rf.rf_layernorm_fused(ins[0], ins[1], ins[2], ins[3], self.o, eps=d["eps"])
 
     def describe(self):
-        d = dict(self.w.dims)
-        return {"workload": self.w.name, **d, "dtype": self.dtype, "seed": self.w.seed}
+        return workload_config(self.w)
 
 
 class L2Flush:
@@ -559,13 +574,13 @@ def main():
             if i >= args.warmup:
                 per_step.append((v, secs))
         val = float(np.mean([v for v, _ in per_step]))
-        unit = "TFLOP/s" if w.kind == "attn" else "GB/s"  # decode, layernorm, rmsnorm, xent, rope: GB/s
+        metric, unit, _ = METRICS[w.kind]
         ms = float(np.mean([s for _, s in per_step]) * 1e3)
         print(json.dumps({
-            "impl": "reference", "metric": "fused cascaded-reduction throughput (CPU fp64 oracle)", "value": val,
+            "impl": "reference", "metric": metric, "value": val,
             "unit": unit, "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, **w.dims, "input_dtype": w.dtype, "seed": w.seed},
+            "config": {**workload_config(w), "parallelism": "single-process (CPU oracle)"},
             "cpu_baseline": {"value": val, "unit": unit, "cores": cpu_threads(), "kind": "oracle", "sample": what},
             "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
         return
