@@ -50,6 +50,9 @@
 // write their normalised partial O_s and lse_s in fp32 to the workspace; the
 // log-sum-exp merge (RedFuser, Figure 13: the FlashDecoding split and merge)
 // then writes those rows of O and LSE.
+// Causal sliding windows of up to kWindowPersistMax keys at D = 64 go to the
+// persistent kernel of attn_fwd_tc_window.cu instead: their units are too short
+// to amortise a CTA each.
 // Every mbarrier wait is bounded; on a timeout the CTA records RF_ERR_TIMEOUT,
 // waits (bounded) for its copies and MMAs in flight, frees TMEM and exits.
 #include <cuda.h>
