@@ -169,6 +169,28 @@ def test_variants(rf, B, H, N, D, window, alibi, dtype):
     check_lse(lse.cpu(), rl, what="variant lse")
 
 
+@pytest.mark.parametrize("dtype,scale,N,window", [
+    ("f16", 0.125, 700, 0),
+    ("bf16", 0.125, 700, 0),
+    ("f16", 1e-3, 700, 0),     # the bias dominates the scores
+    ("f16", 1e-9, 700, 0),     # scores vanish: the bias alone decides
+    ("bf16", 1e-9, 700, 0),
+    ("f16", 0.125, 2600, 1500),  # a wide window (one CTA per unit) with ALiBi
+])
+def test_alibi_across_scales(rf, dtype, scale, N, window):
+    """ALiBi at D = 64 from the usual score scale down to one where the linear
+    bias is all that is left, and with a window too wide for the persistent kernel."""
+    H = 3
+    q, k, v = inputs.attn_inputs(1, H, H, N, N, 64, dtype, seed=N + H)
+    slopes = oracle.alibi_slopes(H)
+    o, lse = rf.attention(q.cuda(), k.cuda(), v.cuda(), scale=scale, causal=True, window=window,
+                          alibi_slopes=torch.tensor(slopes, dtype=torch.float32).cuda())
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention(q, k, v, float(np.float32(scale)), True, window=window, alibi_slopes=slopes)
+    check16(o.cpu(), ro, f"ALiBi {dtype} scale={scale}")
+    check_lse(lse.cpu(), rl, what="ALiBi lse")
+
+
 @pytest.mark.parametrize("window,alibi", [(7, False), (0, True), (40, True)])
 def test_variants_f32_path(rf, window, alibi):
     q, k, v = inputs.attn_inputs(1, 2, 2, 150, 150, 64, "f32", seed=5)
