@@ -15,7 +15,10 @@
 //
 // CTA = two query tiles of 128 rows (rows r0..r0+255 of one (batch, head)),
 // 12 warps:
-//   warp 0      TMA producer: Q once; K and V tiles through 2-3 stage rings.
+//   warp 0      TMA producer: Q once; K and V tiles through 2-3 stage rings
+//               (at D = 64 a stage's K and V share one full/empty barrier
+//               pair, freed once PV_1 of the tile is done: one wait and one
+//               commit fewer per tile on the MMA warp).
 //   warp 1      allocates 512 TMEM columns and issues every tcgen05.mma.
 // Both run their loops as a whole warp with warp-uniform operands; one lane
 // issues through an elect.sync predicate (no divergent branch), which keeps
@@ -197,11 +200,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int jj = 0; jj < n_load; ++jj) {  // ring slot jj holds key tile lo0 + jj
         const int st = jj % S, key0 = (lo0 + jj) * kBN;
         if (jj >= S && !(ok = mbar_wait_warp(&bars->k_empty[st], ((jj / S) - 1) & 1))) break;
-        mbar_expect_tx_elect(&bars->k_full[st], C::kKVBytes);
+        mbar_expect_tx_elect(&bars->k_full[st], C::kSepP ? 2 * C::kKVBytes : C::kKVBytes);
 #pragma unroll
         for (int bx = 0; bx < D / 64; ++bx)
           tma_load_3d_elect(sK + st * C::kKVBytes + bx * (kBN * 128), &tk, &bars->k_full[st], bx * 64, key0, kv_plane);
         ++issued_k;
+        if constexpr (C::kSepP) {  // V rides on K's barriers: one wait and one commit per stage
+#pragma unroll
+          for (int bx = 0; bx < D / 64; ++bx)
+            tma_load_3d_elect(sV + st * C::kKVBytes + bx * (kBN * 128), &tv, &bars->k_full[st], bx * 64, key0, kv_plane);
+          continue;
+        }
         if (jj >= S && !(ok = mbar_wait_warp(&bars->v_empty[st], ((jj / S) - 1) & 1))) break;
         mbar_expect_tx_elect(&bars->v_full[st], C::kKVBytes);
 #pragma unroll
@@ -264,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_s(1, 0);
           tc_commit_elect(&bars->s_full[1]);
         }
-        tc_commit_elect(&bars->k_empty[0]);
+        if constexpr (!C::kSepP) tc_commit_elect(&bars->k_empty[0]);
       }
       int st = 0, ph = 0;  // ring stage and phase of key tile j
       for (int jj = 0; ok && jj < n_load; ++jj) {
@@ -281,7 +290,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_s(0, stn);
             tc_commit_elect(&bars->s_full[0]);
           }
-          if (!(ok = mbar_wait_warp(&bars->v_full[st], ph))) break;
           if (in0(j)) {
             if (!(ok = mbar_wait_warp(&bars->p_ready[0], (j - lo0) & 1))) break;
             tc_fence_after();
@@ -296,7 +304,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_s(1, stn);
             tc_commit_elect(&bars->s_full[1]);
           }
-          if (jn < nt1) tc_commit_elect(&bars->k_empty[stn]);
           if (in1(j)) {
             if (!(ok = mbar_wait_warp(&bars->p_ready[1], (j - lo1) & 1))) break;
             tc_fence_after();
@@ -304,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit_elect(&bars->pv_done[1]);
             if (j == nt1 - 1) tc_commit_elect(&bars->o_final[1]);
           }
-          tc_commit_elect(&bars->v_empty[st]);
+          tc_commit_elect(&bars->k_empty[st]);  // K and V of tile j: both stages free once PV_1(j) is done
         } else {
           // P aliases S: PV_t(j) must be issued before S_t(j+1) overwrites it.
           if (!(ok = mbar_wait_warp(&bars->v_full[st], ph))) break;
