@@ -81,3 +81,18 @@ def test_single_rank_needs_no_collective():
 
     ms, value = bench.aggregate_over_ranks(8.0, 3.0, 1)
     assert ms == 8.0 and value == pytest.approx(3.0 / 8e-3)
+
+
+def test_both_arms_name_every_workload_alike():
+    """The GPU arm and the oracle (reference) arm take metric, unit and the
+    workload part of the config from the same tables, for every workload."""
+    import bench
+    from cascaded_reductions_pass_gb300 import inputs
+
+    for name, w in inputs.WORKLOADS.items():
+        metric, unit, bound = bench.METRICS[w.kind]
+        assert unit in ("TFLOP/s", "GB/s") and bound in ("tensor", "hbm")
+        assert (unit == "TFLOP/s") == (w.kind == "attn")
+        cfg = bench.workload_config(w)
+        assert cfg["workload"] == name and cfg["dtype"] == w.dtype and cfg["seed"] == w.seed
+        assert all(cfg[k] == v for k, v in w.dims.items())
