@@ -529,6 +529,39 @@ def measure_ablations(dev, steps, warmup, flush, peaks):
     return out
 
 
+# The five workload configurations of the headline metric, in their order, then the other workloads.
+CONFIG_ORDER = ["attn_tiny_f32", "attn_fwd_f16_d64", "attn_fwd_causal_gqa_bf16_d128", "decode_splitkv_bf16",
+                "layernorm_residual_bf16"]
+
+
+def _r(x, nd=4):
+    return None if x is None else float(f"{x:.{nd}g}")
+
+
+def compact_summary(head_name, head, head_e2e, parts, ablations):
+    """Every workload's result in a few fields (value, unit, ms per step,
+    roofline fraction and bound, DRAM traffic per launch, end-to-end value),
+    configurations first; and each ablation variant's slowdown against the
+    fused incremental kernel."""
+    allres = {head_name: {**head, "e2e": head_e2e}, **parts}
+    names = [n for n in CONFIG_ORDER if n in allres] + [n for n in allres if n not in CONFIG_ORDER]
+    out = {}
+    for i, n in enumerate(names):
+        r = allres[n]
+        key = f"cfg{CONFIG_ORDER.index(n) + 1} {n}" if n in CONFIG_ORDER else n
+        if "error" in r:
+            out[key] = {"error": r["error"][:80]}
+            continue
+        rl, e = r["roofline"], r.get("e2e") or {}
+        out[key] = {"v": _r(r["value"]), "u": r["unit"], "ms": _r(r["ms_per_step"]),
+                    "frac": _r(rl["frac"], 3), "bound": rl["bound"], "traffic": rl["traffic"],
+                    "e2e": _r(e.get("value"))}
+    if isinstance(ablations, dict) and "error" not in ablations:
+        out["ablation slowdowns"] = {n: [_r(v["slowdown_vs_fused"], 3) for v in a["variants"].values()]
+                                     for n, a in ablations.items()}
+    return out
+
+
 def aggregate_over_ranks(local_ms, units_per_rank, world, device=None):
     """Replicas: every rank processed `units_per_rank`; the job's time is the slowest
     rank's.  Returns (max_ms, whole-job value in units/s).  With world > 1 this is a
@@ -580,7 +613,7 @@ def main():
             "impl": "reference", "metric": metric, "value": val,
             "unit": unit, "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {**workload_config(w), "parallelism": "single-process (CPU oracle)"},
+            "config": workload_config(w), "parallelism": "single-process (CPU oracle)",
             "cpu_baseline": {"value": val, "unit": unit, "cores": cpu_threads(), "kind": "oracle", "sample": what},
             "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
         return
@@ -652,15 +685,18 @@ def main():
             "metric": runner.metric, "value": value, "unit": runner.unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": runner.dtype, "data": "synthetic",
-            "config": {**runner.describe(),
-                       "l2": "flushed before every step, outside the events: 512 MiB memset, then a 256 MiB read "
-                             "so that L2 holds only clean lines",
-                       "parallelism": f"replicas{world}" if world > 1 else "single-gpu"},
+            "config": runner.describe(),
+            "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+            "l2_flush": "before every step, outside the events: 512 MiB memset, then a 256 MiB read "
+                        "so that L2 holds only clean lines",
             "roofline": res["roofline"],
             "e2e": e2e,
             "gpu_launches": launches, "clocks": clocks, "cpu_baseline": cpu,
-            "device_status": int(status), "parts": parts, "ablations": ablations,
+            "device_status": int(status),
             "ms_median": res["ms_median"], "ms_p10": res["ms_p10"], "ms_p90": res["ms_p90"],
+            "parts": parts, "ablations": ablations,
+            # last, so that the end of the line alone carries every workload's result
+            "summary": compact_summary(args.workload, res, e2e, parts, ablations),
         }
         print(json.dumps(line))
     if world > 1:

@@ -563,6 +563,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (!ok) {
       if (lane == 0) atomicOr(status, kStatusTimeout);
       bars->abort = 1;
+      if (piece && row < Nq) {  // a split-tail piece marks its partial row invalid for the merge
+        const long long g = static_cast<long long>(unit - n_full) * (2 * kBM) + (row - r0);
+        lse_part[g * n_split + split] = NAN;
+      }
     }
   }
 

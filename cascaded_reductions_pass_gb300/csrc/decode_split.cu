@@ -25,7 +25,7 @@
 //    with the same rescaling, and the split result is written.
 // Each mbarrier wait is bounded; a wait that runs out sets the device status
 // word, the CTA stops consuming, the producer waits for its copies in flight,
-// and the kernel returns.
+// the split's partials are written as NaN, and the kernel returns.
 #include <cuda.h>
 #include <math.h>
 
@@ -259,7 +259,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   }
   __syncthreads();
-  if (bars->abort) return;
+  if (bars->abort) {
+    // A wait gave up: mark this split's partials invalid (NaN), so that the
+    // merge turns the rows into NaN instead of combining stale slots.
+    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+      const int h = idx / D, d = idx - h * D;
+      const long long row = static_cast<long long>(b) * Hq + hk * G + h;
+      o_part[(row * S + split) * D + d] = NAN;
+      if (d == 0) lse_part[row * S + split] = NAN;
+    }
+    return;
+  }
   for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
     const int h = idx / D, d = idx - h * D;
     float M = -INFINITY;

@@ -6,24 +6,32 @@
 // The cascade mean -> M2 -> normalise runs fused in one pass, in the
 // incremental form of RedFuser (Figure 4): level 2's dependence on level 1 is
 // the additive correction M2 = sum((h - K)^2) - n (mean - K)^2 for any shift
-// K, so with one shift K for the whole row (its first element h_0, which every
-// thread of the row reads) both levels are plain running sums,
+// K, so with one shift K for the whole row both levels are plain running sums,
 // S1 = sum(h - K) and S2 = sum((h - K)^2), updated as each element arrives and
 // merged across lanes (shuffles) and warps (shared memory) with combine op +;
-// then mean = K + S1/n and M2 = S2 - S1^2/n once per row.  The shift keeps
-// that subtraction free of cancellation: K is a sample of the same row, so
-// S1/n is of the order of the row's spread, not of its mean.  (A per-thread
+// then mean - K = S1/n and M2 = S2 - S1^2/n once per row.  (A per-thread
 // shift would need Chan, Golub and LeVeque's pairwise combine of
 // (n, mean, M2) at every merge step; a common shift turns it into two sums,
-// and the per-row merge was this kernel's serial latency.)  The row stays in
-// registers between the statistics and the normalisation, so x and the
-// residual are read from HBM once and y is written once.
+// and the per-row merge was this kernel's serial latency.)
+//
+// Accuracy.  S2 carries rounding of the order of u * S2 = u * (M2 + n d^2),
+// d = mean - K, so the subtraction loses about log2(1 + n d^2 / M2) bits.  K
+// is the mean of the row's first 16-byte vector, which every thread of the row
+// reads: for a row of exchangeable values n d^2 / M2 is then of the order of
+// 1/8 (bf16/f16) or 1/4 (fp32).  When a row still has n d^2 > M2 (an outlier
+// among its first elements), the row takes a second reduction over the values
+// already in registers, M2 = sum((h - K - d)^2), which does not cancel.  With
+// n d^2 <= M2 the one-pass M2 is within a few dozen ulps, and the
+// normalisation uses (h - K) - d, which keeps the large-mean case exact where
+// h - mean, with mean rounded to fp32, would not.  The row stays in registers
+// between the statistics and the normalisation, so x and the residual are read
+// from HBM once and y is written once.
 //
 // The kernel is bound by instruction issue as much as by HBM, so the
 // element-wise work runs on packed fp32 pairs (fma/add/mul .f32x2): three
 // packed operations per pair for the statistics.  The affine map keeps the
-// centred form y = (h - mean) * (gamma * rstd) + beta, so a constant row gives
-// exactly beta.
+// centred form y = ((h - K) - (mean - K)) * (gamma * rstd) + beta; a row of
+// equal values gets K equal to that value, hence exactly beta.
 //
 // Layout: a group of `tpr` threads (a multiple of 32) owns one row; thread t
 // holds the row's 16-byte vectors t, t + tpr, ..., t + (VPT-1)*tpr.  A CTA
@@ -130,8 +138,9 @@ __global__ void __launch_bounds__(1024) ln_fused_kernel(const uint4* __restrict_
     }
   }
 
-  // Levels 1-2, incremental: running sums about the row's first element K
-  // (valid blocks form a prefix i < count; blocks past the row end are skipped).
+  // Levels 1-2, incremental: running sums about K, the mean of the row's first
+  // 16-byte vector (valid blocks form a prefix i < count; blocks past the row
+  // end are skipped).
   float shift = 0.f;
   if (row_ok) {
     uint64_t x0[P], r0[P];
@@ -139,10 +148,18 @@ __global__ void __launch_bounds__(1024) ln_fused_kernel(const uint4* __restrict_
     if (r) {
       V::unpack(__ldg(r + base), r0);
     } else {
-      r0[0] = 0;
+#pragma unroll
+      for (int k = 0; k < P; ++k) r0[k] = 0;
     }
-    float unused;
-    f2unpack(add_f32x2(x0[0], r0[0]), shift, unused);
+    // a pairwise tree, so that a row of equal values gets exactly that value
+    uint64_t hp[P];
+#pragma unroll
+    for (int k = 0; k < P; ++k) hp[k] = add_f32x2(x0[k], r0[k]);
+#pragma unroll
+    for (int w = P / 2; w > 0; w >>= 1)
+#pragma unroll
+      for (int k = 0; k < w; ++k) hp[k] = add_f32x2(hp[k], hp[k + w]);
+    shift = hsum(hp[0]) * (1.0f / (2 * P));
   }
   const uint64_t negk2 = f2pack(-shift, -shift);
   uint64_t h[VPT][P];
@@ -186,13 +203,43 @@ __global__ void __launch_bounds__(1024) ln_fused_kernel(const uint4* __restrict_
     a2 = acc.y;
   }
   const float mean_k = a1 * inv_cols;  // mean - K
-  const float mean = shift + mean_k;
-  const float var = fmaxf(fmaf(-mean_k, mean_k, a2 * inv_cols), 0.f);
+  float var = fmaxf(fmaf(-mean_k, mean_k, a2 * inv_cols), 0.f);
+  const uint64_t negmk2 = f2pack(-mean_k, -mean_k);
+  // Rows whose shift lies more than one standard deviation from their mean
+  // recompute M2 about the mean from registers.  The decision is uniform over
+  // the CTA when rows span several warps (the merge below synchronises it).
+  bool recentre = mean_k * mean_k > var;
+  if (warps_per_row > 1) recentre = __syncthreads_or(recentre);
+  if (recentre) {
+    uint64_t q2 = 0;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      if (t + i * tpr >= nvec) continue;
+#pragma unroll
+      for (int k = 0; k < P; ++k) {
+        const uint64_t e = add_f32x2(add_f32x2(h[i][k], negk2), negmk2);
+        q2 = fma_f32x2(e, e, q2);
+      }
+    }
+    float m2 = hsum(q2);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m2 += __shfl_xor_sync(0xffffffffu, m2, o);
+    if (warps_per_row > 1) {
+      const int w = threadIdx.x >> 5;
+      __syncthreads();  // every thread has read the first merge's values
+      if ((threadIdx.x & 31) == 0) s_warp[w].x = m2;
+      __syncthreads();
+      const int w0 = slot * warps_per_row;
+      m2 = s_warp[w0].x;
+      for (int j = 1; j < warps_per_row; ++j) m2 += s_warp[w0 + j].x;
+    }
+    var = m2 * inv_cols;
+  }
   if (!row_ok) return;
 
-  // Level 3: y = (h - mean) * (gamma * rstd) + beta, three packed ops per pair.
+  // Level 3: y = ((h - K) - (mean - K)) * (gamma * rstd) + beta, four packed ops per pair.
   const float rstd = rsqrtf(var + eps);
-  const uint64_t rstd2 = f2pack(rstd, rstd), negmean2 = f2pack(-mean, -mean);
+  const uint64_t rstd2 = f2pack(rstd, rstd);
   const uint64_t one2 = f2pack(1.f, 1.f), zero2 = 0;
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
@@ -214,7 +261,7 @@ __global__ void __launch_bounds__(1024) ln_fused_kernel(const uint4* __restrict_
 #pragma unroll
     for (int k = 0; k < P; ++k) {
       const uint64_t a = mul_f32x2(g[k], rstd2);
-      y[k] = fma_f32x2(add_f32x2(h[i][k], negmean2), a, b[k]);
+      y[k] = fma_f32x2(add_f32x2(add_f32x2(h[i][k], negk2), negmk2), a, b[k]);
     }
     st_stream(out + base + c, V::pack(y));
     if (r_out) st_stream(r_out + base + c, V::pack(h[i]));

@@ -8,7 +8,15 @@
 // each part's running result by one combine step (RedFuser, Table 1: reduce
 // op + with combine op *; Figure 4, incremental form; Figure 13, the
 // FlashDecoding IR whose split results this merges).  The log-sum-exp is taken
-// relative to max_s lse_s so that no exponential overflows.
+// relative to mx = max_s lse_s so that no exponential overflows, and each
+// weight is formed as exp(lse_s - mx) / sum_s' exp(lse_s' - mx): mx is one of
+// the inputs, so lse_s - mx is exact or nearly so.  exp(lse_s - LSE) would
+// instead carry the rounding of LSE = mx + ln(sum), which is of the order of
+// ulp(LSE) (3e-5 at LSE ~ 500), into every weight as a relative error.
+//
+// A part whose lse_s is NaN (a split kernel that gave up after a bounded wait
+// marks its partials that way) makes the merged row NaN, so a result built
+// from missing partials cannot pass for a valid one.
 //
 // One warp per row: lanes first reduce the parts' LSEs (max, then the sum of
 // exponentials), write the S weights to shared memory, then each lane owns
@@ -61,9 +69,19 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const float
   const float* lp = lse_part + row * S;
 
   float mx = -INFINITY;
-  for (int s = lane; s < S; s += 32) mx = fmaxf(mx, lp[s]);
+  bool bad = false;
+  for (int s = lane; s < S; s += 32) {
+    const float v = lp[s];
+    bad |= v != v;
+    mx = fmaxf(mx, v);
+  }
   mx = warp_max(mx);
   const int D4 = D >> 2;
+  if (__any_sync(0xffffffffu, bad)) {  // a part is marked invalid
+    for (int j = lane; j < D4; j += 32) merge_store4<DT>(o, orow * D4 + j, make_float4(NAN, NAN, NAN, NAN));
+    if (lse && lane == 0) lse[orow] = NAN;
+    return;
+  }
   if (mx == -INFINITY) {  // every part empty
     for (int j = lane; j < D4; j += 32) merge_store4<DT>(o, orow * D4 + j, make_float4(0.f, 0.f, 0.f, 0.f));
     if (lse && lane == 0) lse[orow] = -INFINITY;
@@ -73,7 +91,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const float
   for (int s = lane; s < S; s += 32) sum += expf(lp[s] - mx);
   sum = warp_sum(sum);
   const float L = mx + logf(sum);
-  for (int s = lane; s < S; s += 32) s_w[warp][s] = expf(lp[s] - L);
+  for (int s = lane; s < S; s += 32) s_w[warp][s] = expf(lp[s] - mx) / sum;
   __syncwarp();
   if (lse && lane == 0) lse[orow] = L;
 

@@ -79,17 +79,42 @@ def test_layernorm_golden_fixture(rf):
 
 
 def test_layernorm_large_mean_offset(rf):
-    # Rows with |mean| >> std: the one-pass running M2 must not cancel.
+    # Rows with |mean| >> std: the one-pass running M2 must not cancel, and the
+    # centred value must not carry the rounding of the mean (~3e-5 at 1000,
+    # which is 3e-3 in units of sigma = 0.01).  The fp32 bound holds.
     x, r, g, b = inputs.ln_inputs(8, 4096, "f32", seed=14)
     x = x * 0.01 + 1000.0
     y = run(rf, x, r * 0.0, g, b, 1e-5)
     ref, _ = oracle.layernorm(x, r * 0.0, g, b, 1e-5)
-    # fp32 floor: the mean (~1000) alone rounds by up to 3e-5, which is 3e-3 in units
-    # of sigma = 0.01 (then scaled by gamma <= 1.5).  A one-pass sum-of-squares
-    # variance would lose the 1e-4 variance entirely (errors of order 1).
-    err = float(np.abs(to64(y) - ref).max())
-    assert err <= 1.5e-2, err
-    assert np.linalg.norm(to64(y) - ref) / np.linalg.norm(ref) <= 5e-3
+    check32(y, ref, "large mean")
+
+
+def _rows_with_first_vector(rows, cols, dtype, first, scale=1.0, seed=15):
+    """Rows of N(0, scale^2) whose first 16-byte vector is replaced by `first`
+    (the kernel's shift is that vector's mean)."""
+    x, r, g, b = inputs.ln_inputs(rows, cols, "f32", seed=seed)
+    x = x * scale
+    e = 4 if dtype == "f32" else 8
+    x[:, :e] = first
+    x = x.to(DT[dtype])
+    return x, torch.zeros_like(x), g.to(DT[dtype]), b.to(DT[dtype])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("first,scale,cols", [
+    (1000.0, 0.01, 4096),   # an outlier first vector: the one-pass M2 would cancel
+    (0.9, 1.0, 4096),       # shift 0.9 sigma from the mean: the one-pass branch at its limit
+    (1.1, 1.0, 4096),       # 1.1 sigma: the re-centring branch
+    (40.0, 1.0, 1024),      # one warp per row (several rows per CTA)
+    (40.0, 1.0, 16384),     # 1024 threads per row
+])
+def test_layernorm_shift_far_from_mean(rf, dtype, first, scale, cols):
+    x, r, g, b = _rows_with_first_vector(6, cols, dtype, first, scale)
+    # mix rows that do and do not need the second reduction in one CTA
+    x[1::2] = inputs.ln_inputs(3, cols, dtype, seed=16)[0]
+    y = run(rf, x, r, g, b, 1e-5)
+    ref, _ = oracle.layernorm(x, r, g, b, 1e-5)
+    check(dtype, y, ref, f"shift far from mean ({first}, {scale}, {cols})")
 
 
 @pytest.mark.slow

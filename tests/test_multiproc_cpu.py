@@ -96,3 +96,28 @@ def test_both_arms_name_every_workload_alike():
         cfg = bench.workload_config(w)
         assert cfg["workload"] == name and cfg["dtype"] == w.dtype and cfg["seed"] == w.seed
         assert all(cfg[k] == v for k, v in w.dims.items())
+
+
+def test_compact_summary_names_every_workload_within_the_line_tail():
+    """The bench line ends with a compact summary of every workload (the five
+    configurations first); it must fit in the last ~2 KB of the line."""
+    import json
+
+    import bench
+    from cascaded_reductions_pass_gb300 import inputs
+
+    def fake(name):
+        return {"value": 1234.5678, "unit": "GB/s", "ms_per_step": 0.123456,
+                "roofline": {"frac": 0.912345, "bound": "hbm", "traffic": 2168282112},
+                "e2e": {"value": 187.654321}}
+
+    names = list(inputs.WORKLOADS)
+    head = "attn_fwd_f16_d64"
+    parts = {n: fake(n) for n in names if n != head}
+    abl = {"layernorm_residual_bf16": {"variants": {str(i): {"slowdown_vs_fused": 1.0 + i} for i in range(4)}},
+           "softmax_xent_bf16": {"variants": {str(i): {"slowdown_vs_fused": 1.0 + i} for i in range(3)}}}
+    s = bench.compact_summary(head, fake(head), {"value": 500.0}, parts, abl)
+    keys = list(s)
+    assert keys[:5] == [f"cfg{i + 1} {n}" for i, n in enumerate(bench.CONFIG_ORDER)]
+    assert len(keys) == len(names) + 1
+    assert len(json.dumps({"summary": s})) < 1900

@@ -8,9 +8,9 @@ the middle of a run).  This entry point gives them split-KV decoding with the
 per-split partials kept in scratch built into the library.
 
 The GPU test calls it through the C ABI twice in a row, on two different
-problems, and checks each result against the workspace entry point's within
-the 16-bit tolerances used by every parity test.  This file is named so that
-pytest collects it last.
+problems, and checks each result against the workspace entry point's and
+against the fp64 oracle, within the 16-bit tolerances used by every parity
+test.  This file is named so that pytest collects it last.
 """
 import ctypes
 
@@ -19,6 +19,7 @@ import pytest
 import torch
 
 import cascaded_reductions_pass_gb300 as rfmod
+import oracle
 from cascaded_reductions_pass_gb300 import inputs
 from _parity import check16, check_lse
 
@@ -58,4 +59,7 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(rf):
         torch.cuda.synchronize()
         check16(o.cpu(), o_ref.float().cpu(), f"noalloc vs workspace ({B},{Hq},{L},{D},{S})")
         check_lse(lse.cpu(), lse_ref.cpu(), what="noalloc lse")
+        ro, rl = oracle.decode(q.cpu(), k.cpu(), v.cpu(), scale)
+        check16(o.cpu(), ro, f"noalloc vs oracle ({B},{Hq},{L},{D},{S})")
+        check_lse(lse.cpu(), rl, what="noalloc lse vs oracle")
     assert rf.rf_device_status() == rf.RF_OK
