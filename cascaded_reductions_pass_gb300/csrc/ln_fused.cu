@@ -108,7 +108,14 @@ __device__ __forceinline__ float hsum(uint64_t v) {
   return lo + hi;
 }
 
-template <Dt DT, int VPT>
+// Named barrier over the `count` threads of one row (ids 1..; 0 is __syncthreads).
+__device__ __forceinline__ void row_barrier(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// R_OUT: h = x + r is also written out; otherwise the registers keep h - K,
+// which the normalisation uses directly.
+template <Dt DT, int VPT, bool R_OUT>
 __global__ void __launch_bounds__(1024) ln_fused_kernel(const uint4* __restrict__ x, const uint4* __restrict__ r,
                                                         const uint4* __restrict__ gamma,
                                                         const uint4* __restrict__ beta, uint4* __restrict__ out,
@@ -172,9 +179,10 @@ __global__ void __launch_bounds__(1024) ln_fused_kernel(const uint4* __restrict_
     const bool valid = t + i * tpr < nvec;
 #pragma unroll
     for (int k = 0; k < P; ++k) {
-      h[i][k] = add_f32x2(xp[k], rp[k]);
+      const uint64_t hv = add_f32x2(xp[k], rp[k]);
+      const uint64_t d = add_f32x2(hv, negk2);
+      h[i][k] = R_OUT ? hv : d;
       if (valid) {
-        const uint64_t d = add_f32x2(h[i][k], negk2);
         s1 = add_f32x2(s1, d);
         s2 = fma_f32x2(d, d, s2);
       }
@@ -206,18 +214,17 @@ __global__ void __launch_bounds__(1024) ln_fused_kernel(const uint4* __restrict_
   float var = fmaxf(fmaf(-mean_k, mean_k, a2 * inv_cols), 0.f);
   const uint64_t negmk2 = f2pack(-mean_k, -mean_k);
   // Rows whose shift lies more than one standard deviation from their mean
-  // recompute M2 about the mean from registers.  The decision is uniform over
-  // the CTA when rows span several warps (the merge below synchronises it).
-  bool recentre = mean_k * mean_k > var;
-  if (warps_per_row > 1) recentre = __syncthreads_or(recentre);
-  if (recentre) {
+  // recompute M2 about the mean from registers.  Every thread of a row holds
+  // the same sums, so the decision is uniform over the row; the row's warps
+  // merge through a named barrier of their own, and other rows do not wait.
+  if (mean_k * mean_k > var) {
     uint64_t q2 = 0;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
       if (t + i * tpr >= nvec) continue;
 #pragma unroll
       for (int k = 0; k < P; ++k) {
-        const uint64_t e = add_f32x2(add_f32x2(h[i][k], negk2), negmk2);
+        const uint64_t e = add_f32x2(R_OUT ? add_f32x2(h[i][k], negk2) : h[i][k], negmk2);
         q2 = fma_f32x2(e, e, q2);
       }
     }
@@ -226,9 +233,9 @@ __global__ void __launch_bounds__(1024) ln_fused_kernel(const uint4* __restrict_
     for (int o = 16; o > 0; o >>= 1) m2 += __shfl_xor_sync(0xffffffffu, m2, o);
     if (warps_per_row > 1) {
       const int w = threadIdx.x >> 5;
-      __syncthreads();  // every thread has read the first merge's values
+      row_barrier(1 + slot, tpr);  // the row's threads have read the first merge's values
       if ((threadIdx.x & 31) == 0) s_warp[w].x = m2;
-      __syncthreads();
+      row_barrier(1 + slot, tpr);
       const int w0 = slot * warps_per_row;
       m2 = s_warp[w0].x;
       for (int j = 1; j < warps_per_row; ++j) m2 += s_warp[w0 + j].x;
@@ -237,7 +244,8 @@ __global__ void __launch_bounds__(1024) ln_fused_kernel(const uint4* __restrict_
   }
   if (!row_ok) return;
 
-  // Level 3: y = ((h - K) - (mean - K)) * (gamma * rstd) + beta, four packed ops per pair.
+  // Level 3: y = ((h - K) - (mean - K)) * (gamma * rstd) + beta: three packed
+  // ops per pair from h - K (four when h itself is kept for residual_out).
   const float rstd = rsqrtf(var + eps);
   const uint64_t rstd2 = f2pack(rstd, rstd);
   const uint64_t one2 = f2pack(1.f, 1.f), zero2 = 0;
@@ -261,10 +269,10 @@ __global__ void __launch_bounds__(1024) ln_fused_kernel(const uint4* __restrict_
 #pragma unroll
     for (int k = 0; k < P; ++k) {
       const uint64_t a = mul_f32x2(g[k], rstd2);
-      y[k] = fma_f32x2(add_f32x2(add_f32x2(h[i][k], negk2), negmk2), a, b[k]);
+      y[k] = fma_f32x2(add_f32x2(R_OUT ? add_f32x2(h[i][k], negk2) : h[i][k], negmk2), a, b[k]);
     }
     st_stream(out + base + c, V::pack(y));
-    if (r_out) st_stream(r_out + base + c, V::pack(h[i]));
+    if (R_OUT) st_stream(r_out + base + c, V::pack(h[i]));
   }
 }
 
@@ -374,12 +382,13 @@ cudaError_t launch_dt(const void* x, const void* r, const void* g, const void* b
     else
       rms_fused_kernel<DT, 1><<<gr, threads, 0, s>>>(X, R, G, O, RO, rows, nvec, tpr, inv_cols, eps);
   } else {
-    if (vpt == 4)
-      ln_fused_kernel<DT, 4><<<gr, threads, 0, s>>>(X, R, G, Bt, O, RO, rows, nvec, tpr, inv_cols, eps);
-    else if (vpt == 2)
-      ln_fused_kernel<DT, 2><<<gr, threads, 0, s>>>(X, R, G, Bt, O, RO, rows, nvec, tpr, inv_cols, eps);
-    else
-      ln_fused_kernel<DT, 1><<<gr, threads, 0, s>>>(X, R, G, Bt, O, RO, rows, nvec, tpr, inv_cols, eps);
+#define RF_LN(V_, RO_) ln_fused_kernel<DT, V_, RO_><<<gr, threads, 0, s>>>(X, R, G, Bt, O, RO, rows, nvec, tpr, inv_cols, eps)
+    if (RO) {
+      if (vpt == 4) RF_LN(4, true); else if (vpt == 2) RF_LN(2, true); else RF_LN(1, true);
+    } else {
+      if (vpt == 4) RF_LN(4, false); else if (vpt == 2) RF_LN(2, false); else RF_LN(1, false);
+    }
+#undef RF_LN
   }
   return cudaGetLastError();
 }

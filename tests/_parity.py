@@ -7,6 +7,10 @@ Tolerances (stated once, used everywhere):
   max |gpu - ref| / max |ref| <= 1e-5.
 * LSE (fp32, natural log): max abs error <= 1e-3 on 16-bit paths; on the fp32
   path <= 1e-5 * max(1, max |ref|).
+* 16-bit outputs whose reference reaches |ref| >= 8: there a correctly rounded
+  bf16 value alone can differ from the fp64 reference by up to 2^-5 > 2e-2, so
+  those elements are held to one unit in the last place of the output format
+  instead (check16_wide); every other element keeps max |err| <= 2e-2.
 """
 import numpy as np
 import torch
@@ -54,3 +58,24 @@ def check_lse(out, ref, tol=1e-3, what=""):
     err = float(np.abs(out[fin] - ref[fin]).max()) if fin.any() else 0.0
     assert err <= tol, f"{what}: lse max_abs={err:.3e}"
     return err
+
+
+def ulp16(ref, dtype):
+    """One unit in the last place of the 16-bit format at |ref| (normal range)."""
+    mant = 7 if dtype == torch.bfloat16 else 10
+    a = np.maximum(np.abs(to64(ref)), 2.0 ** -14)
+    return 2.0 ** (np.floor(np.log2(a)) - mant)
+
+
+def check16_wide(out, ref, dtype, what=""):
+    """check16 for outputs that reach |ref| >= 8: those elements within one ulp
+    of the output format, the rest within 2e-2; rel-L2 <= 5e-3 over all."""
+    out64, ref64 = to64(out), to64(ref)
+    assert out64.shape == ref64.shape and np.isfinite(out64).all(), what
+    err = np.abs(out64 - ref64)
+    big = np.abs(ref64) >= 8.0
+    ma = float(err[~big].max()) if (~big).any() else 0.0
+    ul = float((err[big] / ulp16(ref64[big], dtype)).max()) if big.any() else 0.0
+    rl = rel_l2(out64, ref64)
+    assert ma <= 2e-2 and ul <= 1.0 and rl <= 5e-3, f"{what}: max_abs(|ref|<8)={ma:.3e} ulps(|ref|>=8)={ul:.2f} rel_l2={rl:.3e}"
+    return ma, ul, rl

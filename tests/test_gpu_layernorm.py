@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from cascaded_reductions_pass_gb300 import inputs
-from _parity import check16, check32, to64
+from _parity import check16, check16_wide, check32, to64
 from test_golden import dec
 
 pytestmark = pytest.mark.gpu
@@ -114,7 +114,11 @@ def test_layernorm_shift_far_from_mean(rf, dtype, first, scale, cols):
     x[1::2] = inputs.ln_inputs(3, cols, dtype, seed=16)[0]
     y = run(rf, x, r, g, b, 1e-5)
     ref, _ = oracle.layernorm(x, r, g, b, 1e-5)
-    check(dtype, y, ref, f"shift far from mean ({first}, {scale}, {cols})")
+    # the outlier's own output reaches ~64 * gamma: bf16 holds it to one ulp there
+    if dtype == "f32":
+        check32(y, ref, f"shift far from mean ({first}, {scale}, {cols})")
+    else:
+        check16_wide(y, ref, DT[dtype], f"shift far from mean ({first}, {scale}, {cols})")
 
 
 @pytest.mark.slow
