@@ -33,9 +33,11 @@ _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_
 
 
 class AttnOpts(ctypes.Structure):
-    """rf_attn_opts_t: causal mask, sliding window, ALiBi slopes (device fp32 [Hq]), split-tail workspace."""
+    """rf_attn_opts_t: causal mask, sliding window, ALiBi slopes (device fp32 [Hq]), split-tail workspace,
+    rotary embedding inside the kernel (mode, base, position offset)."""
     _fields_ = [("causal", ctypes.c_int), ("window", ctypes.c_int), ("alibi_slopes", ctypes.c_void_p),
-                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("rope", ctypes.c_int), ("rope_base", ctypes.c_float), ("rope_pos_offset", ctypes.c_int)]
 _SIGNATURES = {
     "rf_attn_fwd": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp], _i),
     "rf_attn_fwd_ex": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, ctypes.POINTER(AttnOpts), _i, _vp], _i),
@@ -157,10 +159,11 @@ def rf_attn_fwd(q, k, v, o, lse=None, scale=None, causal=False, stream=None):
 
 
 def rf_attn_fwd_ex(q, k, v, o, lse=None, scale=None, causal=False, window=0, alibi_slopes=None, workspace=None,
-                   stream=None):
+                   stream=None, rope=0, rope_base=10000.0, rope_pos_offset=0):
     """rf_attn_fwd with a sliding window (key j visible iff i - window < j <= i) and/or
-    ALiBi slopes (float32 CUDA tensor [Hq]), both needing causal=True, and an optional
-    workspace (uint8 CUDA tensor, see attn_workspace) for splitting a short last wave."""
+    ALiBi slopes (float32 CUDA tensor [Hq]), both needing causal=True, an optional
+    workspace (uint8 CUDA tensor, see attn_workspace) for splitting a short last wave,
+    and rotary embedding inside the kernel (rope=1: Q rows, rope=2: Q and K rows)."""
     B, Hq, Nq, D = q.shape
     Hkv, Nk = k.shape[1], k.shape[2]
     if tuple(k.shape) != (B, Hkv, Nk, D) or tuple(v.shape) != tuple(k.shape) or tuple(o.shape) != tuple(q.shape):
@@ -174,7 +177,7 @@ def rf_attn_fwd_ex(q, k, v, o, lse=None, scale=None, causal=False, window=0, ali
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
     opts = AttnOpts(int(bool(causal)), int(window), _dev(alibi_slopes, "alibi_slopes", True),
-                    _dev(workspace, "workspace", True), wsb)
+                    _dev(workspace, "workspace", True), wsb, int(rope), float(rope_base), int(rope_pos_offset))
     _check(load().rf_attn_fwd_ex(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(o, "o"), _dev(lse, "lse", True),
                                  B, Hq, Hkv, Nq, Nk, D, scale, ctypes.byref(opts), _code(q.dtype), _stream(stream)))
 
@@ -303,7 +306,8 @@ def alibi_slopes(n_heads, device="cuda"):
 
 
 # ------------------------------------------------------------------ allocating helpers
-def attention(q, k, v, scale=None, causal=False, window=0, alibi_slopes=None, split_tail=True, stream=None):
+def attention(q, k, v, scale=None, causal=False, window=0, alibi_slopes=None, split_tail=True, stream=None,
+              rope=0, rope_base=10000.0, rope_pos_offset=0):
     """Allocate (o, lse) and run rf_attn_fwd_ex; with split_tail (the default) a short last
     wave of the unmasked 16-bit kernel is split along the keys (a workspace is allocated)."""
     o = torch.empty_like(q)
@@ -312,7 +316,7 @@ def attention(q, k, v, scale=None, causal=False, window=0, alibi_slopes=None, sp
     if split_tail and not causal and q.dtype != torch.float32:
         ws = attn_workspace(q, k, causal)
     rf_attn_fwd_ex(q, k, v, o, lse, scale=scale, causal=causal, window=window, alibi_slopes=alibi_slopes,
-                   workspace=ws, stream=stream)
+                   workspace=ws, stream=stream, rope=rope, rope_base=rope_base, rope_pos_offset=rope_pos_offset)
     return o, lse
 
 

@@ -1,666 +1,9 @@
-// attn_fwd_tc.cu -- attention forward on the 5th-generation tensor cores
-// (tcgen05 + TMEM + TMA) for fp16/bf16 inputs, D in {64, 128}.
-//
-// The cascade max -> sum exp -> sum exp*v (RedFuser, Abstract: safe softmax
-// followed by GEMM; "Operator Fusion" guide, section 2, Pattern 4) runs as one
-// loop over 128-key tiles in the incremental form of RedFuser's Figure 4:
-// level 1 (reduce max, combine +) keeps a running row max m; levels 2 and 3
-// (reduce +, combine *) keep the running sum l and the running output O, both
-// corrected by exp(m_old - m_new) when m rises.  The correction is applied
-// lazily, which stays exact because l and O are always built against the same
-// m: m moves only when a tile's max exceeds it by more than 2^8 (in base 2),
-// which keeps P <= 256.  Non-causal D = 64 rows speculate: once m is finite, P
-// is formed against it without scanning the tile, and m moves only when a half
-// row's sum of P exceeds 2^15, so P stays <= 2^15.
-//
-// CTA = two query tiles of 128 rows (rows r0..r0+255 of one (batch, head)),
-// 12 warps:
-//   warp 0      TMA producer: Q once; K and V tiles through 2-3 stage rings
-//               (at D = 64 a stage's K and V share one full/empty barrier
-//               pair, freed once PV_1 of the tile is done: one wait and one
-//               commit fewer per tile on the MMA warp).
-//   warp 1      allocates 512 TMEM columns and issues every tcgen05.mma.
-// Both run their loops as a whole warp with warp-uniform operands; one lane
-// issues through an elect.sync predicate (no divergent branch), which keeps
-// the issue cost at the tensor core's own rate.
-//   warps 4-7   softmax for query tile 0, warps 8-11 for tile 1: one thread
-//               per query row, i.e. per TMEM lane, so row max and row sum need
-//               no cross-thread reduction.
-// Registers are re-split after launch: warps 0-3 drop to 80 per thread and
-// the softmax warps rise to 208 (a row of S is 128 registers).
-//
-// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D).
-//  * D = 64: P0 [384,448) and P1 [448,512) have columns of their own (16-bit,
-//    two per column).  Softmax frees S_t as soon as it has loaded it, so the
-//    MMA issuer runs S_t(j+1) while softmax still exponentiates tile j; PV_t(j)
-//    follows once P_t(j) is ready.  Softmax waits for PV_t(j-1) to complete
-//    before it overwrites P_t or rescales O_t.
-//  * D = 128: no spare columns; P_t overwrites the first 64 columns of S_t and
-//    the order per key tile is PV0_j, S0_{j+1}, PV1_j, S1_{j+1}, so the tensor
-//    core works on one tile while the other tile's softmax runs (ping-pong).
-//    A commit after S_t(j+1) then also covers PV_t(j).
-// In both cases P is the TMEM A operand of O += P V.
-//
-// Shared memory operands use the 128-byte swizzle written by TMA: Q and K
-// K-major (boxes of 64 dims x 128 rows), V MN-major (the same boxes read as
-// D x keys).  Causal CTAs are scheduled longest-first, and the query heads of
-// one GQA group are adjacent in launch order so their K/V tiles hit in L2.
-//
-// Split tail (no mask, caller workspace given): with one CTA per SM, U units
-// of 256 query rows take ceil(U / SMs) waves, and a last wave of a few units
-// leaves most SMs idle for a whole unit.  The last U mod SMs units are then
-// split along the keys into n_split pieces each (one CTA per piece), which
-// write their normalised partial O_s and lse_s in fp32 to the workspace; the
-// log-sum-exp merge (RedFuser, Figure 13: the FlashDecoding split and merge)
-// then writes those rows of O and LSE.
-// Causal sliding windows of up to kWindowPersistMax keys at D = 64 go to the
-// persistent kernel of attn_fwd_tc_window.cu instead: their units are too short
-// to amortise a CTA each.
-// Every mbarrier wait is bounded; on a timeout the CTA records RF_ERR_TIMEOUT,
-// waits (bounded) for its copies and MMAs in flight, frees TMEM and exits.
-#include <cuda.h>
-#include <math.h>
-
-#include "attn_tc_common.cuh"
-#include "lse_merge.cuh"
-#include "rf_device.cuh"
+// attn_fwd_tc.cu -- the tensor-core attention forward without rotary
+// embedding (the kernel template is in attn_fwd_tc.cuh), the split-tail
+// workspace size, and the dispatch of every 16-bit attention call.
+#include "attn_fwd_tc.cuh"
 
 namespace rf {
-namespace {
-
-// Speculative P (rows with a finite running max): every P of a half row stays
-// <= 2^kSpecLog2, far inside fp16's range, or the half is redone.
-constexpr float kSpecLog2 = 15.0f;
-constexpr float kSpecMax = 32768.0f;  // 2^kSpecLog2
-
-template <int D>
-struct Cfg {
-  static constexpr int kQBytes = kBM * D * 2;    // one query tile
-  static constexpr int kKVBytes = kBN * D * 2;   // one K or V tile
-  static constexpr int kStages = D == 64 ? 3 : 2;
-  static constexpr int kTiles = 2 * kQBytes + 2 * kStages * kKVBytes;
-  static constexpr bool kSepP = D == 64;         // P in columns of its own
-  static constexpr int kOCol = 2 * kBN;          // O0 at 256, O1 at 256 + D
-  static constexpr int kPCol = 2 * kBN + 2 * D;  // P0 at 384, P1 at 448 (D = 64)
-};
-
-struct alignas(8) TcBars {
-  uint64_t q_full;
-  uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];
-  uint64_t s_full[2], s_free[2], p_ready[2], pv_done[2], o_final[2];
-  uint64_t drain;
-  uint32_t tmem_base;
-  int abort;
-};
-
-// Output rows of the split tail's partial rows (partial row g = row g % 256 of
-// tail unit g / 256); rows past Nq are skipped.
-struct AttnTailRows {
-  int first_unit, BH, nqt, Nq;
-  __device__ __forceinline__ long long operator()(long long g) const {
-    int c, bh;
-    unit_coords(first_unit + static_cast<int>(g / (2 * kBM)), BH, nqt, c, bh);
-    const int q = c * 2 * kBM + static_cast<int>(g % (2 * kBM));
-    return q < Nq ? static_cast<long long>(bh) * Nq + q : -1;
-  }
-};
-
-// MASK: 0 none, 1 causal (top-left), 2 causal with a sliding window of
-// `window` keys (key j visible to query i iff i - window < j <= i).
-// ALIBI: add slope_h * (j - i) to each scaled score (slopes per query head).
-template <Dt DT, int D, int MASK, bool ALIBI>
-__global__ void __launch_bounds__(kThreads, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                   const __grid_constant__ CUtensorMap tv, uint16_t* __restrict__ o, float* __restrict__ lse,
-                   int Hq, int Hkv, int Nq, int Nk, int BH, int nqt, float sl2, int window,
-                   const float* __restrict__ alibi, unsigned* status, int n_full, int n_split,
-                   float* __restrict__ o_part, float* __restrict__ lse_part) {
-  constexpr bool CAUSAL = MASK >= 1;
-  constexpr bool kSpec = D == 64 && MASK == 0 && !ALIBI;
-  using C = Cfg<D>;
-  constexpr int S = C::kStages;
-  constexpr bool kBF16 = DT == Dt::BF16;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sK = sQ + 2 * C::kQBytes;
-  uint8_t* sV = sK + S * C::kKVBytes;
-  TcBars* bars = reinterpret_cast<TcBars*>(sV + S * C::kKVBytes);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // CTAs from n_full on are pieces of the split tail: piece p is key range
-  // p % n_split of unit n_full + p / n_split.
-  const int id = blockIdx.x;
-  const bool piece = MASK == 0 && id >= n_full;
-  const int unit = piece ? n_full + (id - n_full) / n_split : id;
-  const int split = piece ? (id - n_full) % n_split : 0;
-  int c, bh;
-  unit_coords(unit, BH, nqt, c, bh);
-  const int h = bh % Hq, b = bh / Hq;
-  const int kv_plane = b * Hkv + h / (Hq / Hkv);
-  const int r0 = c * 2 * kBM;
-  // Key tiles [lo_t, nt_t) that query tile t can see; the CTA streams
-  // [lo0, nt1) (tile 1's rows come after tile 0's, so lo0 <= lo1, nt0 <= nt1).
-  const int n_kv = (Nk + kBN - 1) / kBN;
-  // a piece's key tiles: [floor(split n_kv / n_split), floor((split + 1) n_kv / n_split)), never empty
-  const int plo = piece ? static_cast<int>(static_cast<long long>(split) * n_kv / n_split) : 0;
-  const int phi = piece ? static_cast<int>(static_cast<long long>(split + 1) * n_kv / n_split) : n_kv;
-  const int nt0 = CAUSAL ? min(r0 / kBN + 1, n_kv) : phi;
-  const int nt1 = CAUSAL ? min(r0 / kBN + 2, n_kv) : phi;
-  const int lo0 = MASK == 2 ? max(0, r0 - window + 1) / kBN : plo;
-  const int lo1 = MASK == 2 ? max(0, r0 + kBM - window + 1) / kBN : plo;
-  const int n_load = nt1 - lo0;
-
-  if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
-    for (int i = 0; i < S; ++i) {
-      mbar_init(&bars->k_full[i], 1);
-      mbar_init(&bars->k_empty[i], 1);
-      mbar_init(&bars->v_full[i], 1);
-      mbar_init(&bars->v_empty[i], 1);
-    }
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->s_free[t], 4 * 32);
-      mbar_init(&bars->p_ready[t], 4 * 32);
-      mbar_init(&bars->pv_done[t], 1);
-      mbar_init(&bars->o_final[t], 1);
-    }
-    mbar_init(&bars->drain, 1);
-    bars->abort = 0;
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tc_alloc(&bars->tmem_base, kTmemCols);
-    tc_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = bars->tmem_base;
-
-  // Register split: 128 x 80 (producer / MMA warpgroup) + 256 x 208 (softmax)
-  // = 63,488 <= 384 x 168 registers granted at launch.
-  static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= kThreads * 168, "register split exceeds the launch budget");
-  if (warp < 4) {
-    regs_dec<kRegsCtl>();
-    if (warp == 0) {
-      // ---------------------------------------------------------- TMA producer (whole warp, one lane issues)
-      tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tk);
-      tma_prefetch_desc(&tv);
-      mbar_expect_tx_elect(&bars->q_full, 2 * C::kQBytes);
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-#pragma unroll
-        for (int bx = 0; bx < D / 64; ++bx)
-          tma_load_3d_elect(sQ + t * C::kQBytes + bx * (kBM * 128), &tq, &bars->q_full, bx * 64, r0 + t * kBM, bh);
-      int issued_k = 0, issued_v = 0;
-      bool ok = true;
-      for (int jj = 0; jj < n_load; ++jj) {  // ring slot jj holds key tile lo0 + jj
-        const int st = jj % S, key0 = (lo0 + jj) * kBN;
-        if (jj >= S && !(ok = mbar_wait_warp(&bars->k_empty[st], ((jj / S) - 1) & 1))) break;
-        mbar_expect_tx_elect(&bars->k_full[st], C::kSepP ? 2 * C::kKVBytes : C::kKVBytes);
-#pragma unroll
-        for (int bx = 0; bx < D / 64; ++bx)
-          tma_load_3d_elect(sK + st * C::kKVBytes + bx * (kBN * 128), &tk, &bars->k_full[st], bx * 64, key0, kv_plane);
-        ++issued_k;
-        if constexpr (C::kSepP) {  // V rides on K's barriers: one wait and one commit per stage
-#pragma unroll
-          for (int bx = 0; bx < D / 64; ++bx)
-            tma_load_3d_elect(sV + st * C::kKVBytes + bx * (kBN * 128), &tv, &bars->k_full[st], bx * 64, key0, kv_plane);
-          continue;
-        }
-        if (jj >= S && !(ok = mbar_wait_warp(&bars->v_empty[st], ((jj / S) - 1) & 1))) break;
-        mbar_expect_tx_elect(&bars->v_full[st], C::kKVBytes);
-#pragma unroll
-        for (int bx = 0; bx < D / 64; ++bx)
-          tma_load_3d_elect(sV + st * C::kKVBytes + bx * (kBN * 128), &tv, &bars->v_full[st], bx * 64, key0, kv_plane);
-        ++issued_v;
-      }
-      if (!ok) {
-        if (lane == 0) atomicOr(status, kStatusTimeout);
-        bars->abort = 1;
-      }
-      // every copy issued must land before the CTA exits
-      bool drained = mbar_wait_warp(&bars->q_full, 0);
-      for (int j = issued_k > S ? issued_k - S : 0; j < issued_k; ++j)
-        drained &= mbar_wait_warp(&bars->k_full[j % S], (j / S) & 1);
-      for (int j = issued_v > S ? issued_v - S : 0; j < issued_v; ++j)
-        drained &= mbar_wait_warp(&bars->v_full[j % S], (j / S) & 1);
-      if (!drained && lane == 0) atomicOr(status, kStatusTimeout);
-    } else if (warp == 1) {
-      // ---------------------------------------------------------- MMA issuer (whole warp, one lane issues)
-      // Issue cost matters here (one lane issues every MMA), so the whole warp
-      // runs this loop with warp-uniform operands and elect.sync predicates the
-      // instructions; the shared memory descriptors are built once: a K-step or
-      // a ring stage only moves the 14-bit start-address field.
-      constexpr uint32_t idS = tc_idesc_f16(kBF16, kBM, kBN, false);
-      constexpr uint32_t idPV = tc_idesc_f16(kBF16, kBM, D, true);
-      const uint64_t dQ = tc_sdesc_sw128(smem_u32(sQ), 16, 1024);
-      const uint64_t dK = tc_sdesc_sw128(smem_u32(sK), 16, 1024);
-      const uint64_t dV = tc_sdesc_sw128(smem_u32(sV), kBN * 128, 1024);
-      auto issue_s = [&](int t, int st) {  // S_t = Q_t K^T from K stage st  (M=128, N=128, K=D)
-        const uint64_t a0 = dQ + static_cast<uint64_t>(t * (C::kQBytes >> 4));
-        const uint64_t b0 = dK + static_cast<uint64_t>(st * (C::kKVBytes >> 4));
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          constexpr int kStepQ = kBM * 128 / 16, kStepK = kBN * 128 / 16;  // one 64-dim box
-          const uint32_t oq = (kk >> 2) * kStepQ + (kk & 3) * 2, ok_ = (kk >> 2) * kStepK + (kk & 3) * 2;
-          tc_mma_ss_elect(tmem + t * kBN, a0 + oq, b0 + ok_, idS, kk > 0 ? 1u : 0u);
-        }
-      };
-      auto issue_pv = [&](int t, int st, bool acc) {  // O_t += P_t V from V stage st  (M=128, N=D, K=128)
-        const uint64_t b0 = dV + static_cast<uint64_t>(st * (C::kKVBytes >> 4));
-        const uint32_t pcol = tmem + (C::kSepP ? C::kPCol + t * (kBN / 2) : t * kBN);
-        const uint32_t dO = tmem + C::kOCol + t * D;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          tc_mma_ts_elect(dO, pcol + kk * 8, b0 + kk * (16 * 128 / 16), idPV, (acc || kk > 0) ? 1u : 0u);
-      };
-      // Key tile j (ring slot jj = j - lo0) feeds query tile t when lo_t <= j < nt_t;
-      // barrier phases of tile t count its own key tiles (j - lo_t).
-      auto in0 = [&](int j) { return j >= lo0 && j < nt0; };
-      auto in1 = [&](int j) { return j >= lo1 && j < nt1; };
-      bool ok = mbar_wait_warp(&bars->q_full, 0) && mbar_wait_warp(&bars->k_full[0], 0);
-      if (ok) {
-        tc_fence_after();
-        if (in0(lo0)) {
-          issue_s(0, 0);
-          tc_commit_elect(&bars->s_full[0]);
-        }
-        if (in1(lo0)) {
-          issue_s(1, 0);
-          tc_commit_elect(&bars->s_full[1]);
-        }
-        if constexpr (!C::kSepP) tc_commit_elect(&bars->k_empty[0]);
-      }
-      int st = 0, ph = 0;  // ring stage and phase of key tile j
-      for (int jj = 0; ok && jj < n_load; ++jj) {
-        const int j = lo0 + jj, jn = j + 1;
-        const int stn = st + 1 == S ? 0 : st + 1, phn = st + 1 == S ? ph ^ 1 : ph;  // stage / phase of j+1
-        bool k_ready = false;
-        if constexpr (C::kSepP) {
-          // S_t(j+1) as soon as softmax t has read S_t(j); PV_t(j) once P_t(j) is ready.
-          if (in0(jn)) {
-            if (jn > lo0 && !(ok = mbar_wait_warp(&bars->s_free[0], (jn - 1 - lo0) & 1))) break;
-            if (!(ok = mbar_wait_warp(&bars->k_full[stn], phn))) break;
-            k_ready = true;
-            tc_fence_after();
-            issue_s(0, stn);
-            tc_commit_elect(&bars->s_full[0]);
-          }
-          if (in0(j)) {
-            if (!(ok = mbar_wait_warp(&bars->p_ready[0], (j - lo0) & 1))) break;
-            tc_fence_after();
-            issue_pv(0, st, j > lo0);
-            tc_commit_elect(&bars->pv_done[0]);
-            if (j == nt0 - 1) tc_commit_elect(&bars->o_final[0]);
-          }
-          if (in1(jn)) {
-            if (jn > lo1 && !(ok = mbar_wait_warp(&bars->s_free[1], (jn - 1 - lo1) & 1))) break;
-            if (!k_ready && !(ok = mbar_wait_warp(&bars->k_full[stn], phn))) break;
-            tc_fence_after();
-            issue_s(1, stn);
-            tc_commit_elect(&bars->s_full[1]);
-          }
-          if (in1(j)) {
-            if (!(ok = mbar_wait_warp(&bars->p_ready[1], (j - lo1) & 1))) break;
-            tc_fence_after();
-            issue_pv(1, st, j > lo1);
-            tc_commit_elect(&bars->pv_done[1]);
-            if (j == nt1 - 1) tc_commit_elect(&bars->o_final[1]);
-          }
-          tc_commit_elect(&bars->k_empty[st]);  // K and V of tile j: both stages free once PV_1(j) is done
-        } else {
-          // P aliases S: PV_t(j) must be issued before S_t(j+1) overwrites it.
-          if (!(ok = mbar_wait_warp(&bars->v_full[st], ph))) break;
-          if (in0(j)) {
-            if (!(ok = mbar_wait_warp(&bars->p_ready[0], (j - lo0) & 1))) break;
-            tc_fence_after();
-            issue_pv(0, st, j > lo0);
-            if (j == nt0 - 1) tc_commit_elect(&bars->o_final[0]);
-          }
-          if (in0(jn)) {
-            if (!(ok = mbar_wait_warp(&bars->k_full[stn], phn))) break;
-            k_ready = true;
-            tc_fence_after();
-            issue_s(0, stn);
-            tc_commit_elect(&bars->s_full[0]);
-          }
-          if (in1(j)) {
-            if (!(ok = mbar_wait_warp(&bars->p_ready[1], (j - lo1) & 1))) break;
-            tc_fence_after();
-            issue_pv(1, st, j > lo1);
-            if (j == nt1 - 1) tc_commit_elect(&bars->o_final[1]);
-          }
-          tc_commit_elect(&bars->v_empty[st]);
-          if (in1(jn)) {
-            if (!k_ready) {
-              if (!(ok = mbar_wait_warp(&bars->k_full[stn], phn))) break;
-              tc_fence_after();
-            }
-            issue_s(1, stn);
-            tc_commit_elect(&bars->s_full[1]);
-          }
-          if (jn < nt1) tc_commit_elect(&bars->k_empty[stn]);
-        }
-        st = stn;
-        ph = phn;
-      }
-      if (!ok) {
-        if (lane == 0) atomicOr(status, kStatusTimeout);
-        bars->abort = 1;
-      }
-      // every MMA issued must complete before TMEM is released
-      tc_commit_elect(&bars->drain);
-      if (!mbar_wait_warp(&bars->drain, 0) && lane == 0) atomicOr(status, kStatusTimeout);
-    }
-  } else {
-    regs_inc<kRegsSoftmax>();
-    // ------------------------------------------------------------ softmax (one thread per query row)
-    const int t = (warp - 4) >> 2;
-    const int qw = warp & 3;
-    const int row = r0 + t * kBM + qw * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
-    const uint32_t tS = tmem + lane_off + t * kBN;
-    const uint32_t tP = tmem + lane_off + (C::kSepP ? C::kPCol + t * (kBN / 2) : t * kBN);
-    const uint32_t tO = tmem + lane_off + C::kOCol + t * D;
-    const int jlo = t == 0 ? lo0 : lo1, jhi = t == 0 ? nt0 : nt1;
-    const uint64_t sl2x2 = f2pack(sl2, sl2);
-    const float slope2 = ALIBI ? __ldg(alibi + (bh % Hq)) * kLog2e : 0.f;
-    float m_run = -INFINITY, l_run = 0.f;
-    bool spec = kSpec;  // warp-uniform: cleared by the first failed speculation
-    bool ok = true;
-    for (int j = jlo; j < jhi; ++j) {
-      const int jt = j - jlo;  // this tile's own key-tile count: barrier phases
-      if (!(ok = warp_wait(&bars->s_full[t], jt & 1))) break;
-      tc_fence_after();
-      uint32_t s[kBN];
-#pragma unroll
-      for (int i = 0; i < kBN / 32; ++i) tc_ld32(tS + 32 * i, s + 32 * i);
-      tc_wait_ld();
-      if constexpr (C::kSepP) {  // S_t may be overwritten by S_t(j+1) now
-        tc_fence_before();
-        mbar_arrive(&bars->s_free[t]);
-      }
-      const int key0 = j * kBN;
-      if constexpr (CAUSAL) {
-        // columns below cl and from cf on are visible; each bound costs one
-        // compare per column only where some row of the warp needs it
-        const int cl = min(Nk, row + 1) - key0;
-        if (__any_sync(0xffffffffu, cl < kBN)) {
-#pragma unroll
-          for (int c = 0; c < kBN; ++c)
-            if (c >= cl) s[c] = __float_as_uint(-INFINITY);
-        }
-        if constexpr (MASK == 2) {
-          const int cf = row - window + 1 - key0;
-          if (__any_sync(0xffffffffu, cf > 0)) {
-#pragma unroll
-            for (int c = 0; c < kBN; ++c)
-              if (c < cf) s[c] = __float_as_uint(-INFINITY);
-          }
-        }
-      } else if (key0 + kBN > Nk) {
-        const int lim = Nk, first = 0;  // keys below lim and from first on are visible
-#pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          if (key0 + c >= lim || key0 + c < first) s[c] = __float_as_uint(-INFINITY);
-      }
-      if constexpr (ALIBI) {
-        // s <- s * scale * log2 e + slope * log2 e * (key - row), one packed FMA per
-        // pair: the bias of the pair (2e, 2e+1) rides in one of four packed
-        // accumulators that advance by 8 * slope per pair of their own.
-        const float base = slope2 * static_cast<float>(key0 - row);
-        uint64_t bias[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          bias[k] = f2pack(fmaf(slope2, static_cast<float>(2 * k), base),
-                           fmaf(slope2, static_cast<float>(2 * k + 1), base));
-        const uint64_t step = f2pack(8.f * slope2, 8.f * slope2);
-#pragma unroll
-        for (int e = 0; e < kBN / 2; ++e) {
-          const uint64_t r = fma_f32x2(u2pack(s[2 * e], s[2 * e + 1]), sl2x2, bias[e & 3]);
-          f2unpack_u(r, s[2 * e], s[2 * e + 1]);
-          bias[e & 3] = add_f32x2(bias[e & 3], step);
-        }
-      }
-      uint32_t pk[kBN / 2];
-      float m_new = m_run, tsum = 0.f;
-      bool need = false;
-      // Speculation (non-causal D = 64 without ALiBi): a row whose running max m
-      // is finite first forms P against m without scanning the tile, which is
-      // exact as long as no P exceeds kSpecMax; the sum of each half row bounds
-      // that.  When a first half fails, the row is redone from the tile max;
-      // when only a second half fails, that half is rescanned alone.  After one
-      // failure the warp stops speculating (steadily rising scores would make
-      // it fail on every tile).
-      if constexpr (kSpec) {
-        bool exact = !spec || __any_sync(0xffffffffu, m_run == -INFINITY);
-        float h0, h1;
-        for (;;) {
-          if (exact) {
-            const float mt = scaled_max_from<0, ALIBI>(s, sl2);
-            m_new = mt > m_run + kRescaleThreshold ? mt : m_run;
-          }
-          const float m_use = m_new == -INFINITY ? 0.f : m_new;
-          const uint64_t negm2 = f2pack(-m_use, -m_use);
-          h0 = exp_pairs<DT, ALIBI, 0, kBN / 4>(s, sl2x2, negm2, pk);
-          if (exact) {
-            h1 = exp_pairs<DT, ALIBI, kBN / 4, kBN / 2>(s, sl2x2, negm2, pk);
-            break;
-          }
-          if (!__any_sync(0xffffffffu, !(h0 <= kSpecMax))) {
-            h1 = exp_pairs<DT, ALIBI, kBN / 4, kBN / 2>(s, sl2x2, negm2, pk);
-            const bool big = !(h1 <= kSpecMax);
-            if (__any_sync(0xffffffffu, big)) {
-              // every first-half P is <= 2^kSpecLog2, so m + kSpecLog2 bounds that half
-              spec = false;
-              const float mt = scaled_max_from<kBN / 2, ALIBI>(s, sl2);
-              m_new = big ? fmaxf(mt, m_run + kSpecLog2) : m_run;
-              const float a = ex2_ftz(m_run - m_new);
-#pragma unroll
-              for (int e = 0; e < kBN / 4; ++e) pk[e] = scale_pair<DT>(pk[e], a);
-              h0 *= a;
-              h1 = exp_pairs<DT, ALIBI, kBN / 4, kBN / 2>(s, sl2x2, f2pack(-m_new, -m_new), pk);
-            }
-            break;
-          }
-          exact = true;  // a first half failed: redo the row from the tile max
-          spec = false;
-        }
-        need = m_new != m_run && m_new != -INFINITY;
-        tsum = h0 + h1;
-      } else {
-        // level 1: the tile max over the row decides m; level 2: P = 2^(s*sl2 - m)
-        const float mt = scaled_max_from<0, ALIBI>(s, sl2);
-        need = mt > m_run + kRescaleThreshold;
-        m_new = need ? mt : m_run;
-        // a row can see no key of this tile (sliding window): keep it at zero weight
-        const float m_use = m_new == -INFINITY ? 0.f : m_new;
-        tsum = exp_pairs<DT, ALIBI, 0, kBN / 2>(s, sl2x2, f2pack(-m_use, -m_use), pk);
-      }
-      // all exponentials run before any wait below
-      const float alpha = need ? ex2_ftz(m_run - m_new) : 1.f;
-      if constexpr (C::kSepP) {  // PV_t(j-1) must be done before P_t and O_t are touched
-        if (jt > 0) {
-          if (!(ok = warp_wait(&bars->pv_done[t], (jt - 1) & 1))) break;
-          tc_fence_after();
-        }
-      }
-#pragma unroll
-      for (int cc = 0; cc < kBN / 16; ++cc) tc_st8(tP + 8 * cc, pk + 8 * cc);
-      l_run = fmaf(l_run, alpha, tsum);
-      // level 3 correction: rescale O in TMEM when some row's max moved
-      if (jt > 0 && __any_sync(0xffffffffu, need)) {
-        const uint64_t a2 = f2pack(alpha, alpha);
-#pragma unroll
-        for (int i = 0; i < D / 32; ++i) {
-          uint32_t ov[32];
-          tc_ld32(tO + 32 * i, ov);
-          tc_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const uint64_t r = mul_f32x2(u2pack(ov[e], ov[e + 1]), a2);
-            f2unpack_u(r, ov[e], ov[e + 1]);
-          }
-          tc_st32(tO + 32 * i, ov);
-        }
-      }
-      m_run = m_new;
-      tc_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars->p_ready[t]);
-    }
-    // A sliding window can leave query tile 1 of the last unit without any key
-    // tile, when all its rows lie past Nq (every row below Nq sees its own key):
-    // then no PV is issued for it and it has nothing to write.
-    const bool has_keys = jhi > jlo;
-    if (ok && has_keys) ok = warp_wait(&bars->o_final[t], 0);
-    if (ok && has_keys) {
-      // epilogue: O / l in the output dtype, LSE in natural log
-      tc_fence_after();
-      const float inv = 1.0f / l_run;
-      const bool row_ok = row < Nq;
-      if (piece) {  // partial row g of the split tail: O_s and lse_s in fp32
-        const long long g = static_cast<long long>(unit - n_full) * (2 * kBM) + (row - r0);
-        float4* prow = reinterpret_cast<float4*>(o_part + (g * n_split + split) * D);
-#pragma unroll
-        for (int i = 0; i < D / 32; ++i) {
-          uint32_t ov[32];
-          tc_ld32(tO + 32 * i, ov);
-          tc_wait_ld();
-          if (row_ok) {
-#pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4)
-              prow[i * 8 + v4] =
-                  make_float4(__uint_as_float(ov[4 * v4]) * inv, __uint_as_float(ov[4 * v4 + 1]) * inv,
-                              __uint_as_float(ov[4 * v4 + 2]) * inv, __uint_as_float(ov[4 * v4 + 3]) * inv);
-          }
-        }
-        if (row_ok) lse_part[g * n_split + split] = (m_run + log2f(l_run)) * kLn2;
-      } else {
-        uint4* orow =
-            reinterpret_cast<uint4*>(o + (static_cast<long long>(bh) * Nq + (row_ok ? row : 0)) * D);
-#pragma unroll
-        for (int i = 0; i < D / 32; ++i) {
-          uint32_t ov[32];
-          tc_ld32(tO + 32 * i, ov);
-          tc_wait_ld();
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = Pack<DT>::pack2(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
-          if (row_ok) {
-#pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              orow[i * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-          }
-        }
-        if (row_ok && lse) lse[static_cast<long long>(bh) * Nq + row] = (m_run + log2f(l_run)) * kLn2;
-      }
-    } else if (!ok) {
-      if (lane == 0) atomicOr(status, kStatusTimeout);
-      bars->abort = 1;
-      if (piece && row < Nq) {  // a split-tail piece marks its partial row invalid for the merge
-        const long long g = static_cast<long long>(unit - n_full) * (2 * kBM) + (row - r0);
-        lse_part[g * n_split + split] = NAN;
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tc_dealloc(tmem, kTmemCols);
-  }
-}
-
-// Split-tail plan: the last `tail` = units mod sms units become n_split pieces
-// each (n_split = min(sms / tail, key tiles) >= 2), else nothing is split.
-struct TailPlan {
-  long long n_full;
-  int tail, n_split;
-};
-
-TailPlan tail_plan(long long units, int n_kv, int sms) {
-  const int tail = sms > 0 ? static_cast<int>(units % sms) : 0;
-  const int n_split = tail > 0 ? min(sms / tail, n_kv) : 1;
-  if (tail == 0 || n_split < 2) return TailPlan{units, 0, 1};
-  return TailPlan{units - tail, tail, n_split};
-}
-
-// Workspace layout of a split tail: o_part [tail * 256, n_split, D] fp32, then
-// lse_part [tail * 256, n_split] fp32 at the next 256-byte boundary.
-size_t tail_o_bytes(const TailPlan& p, int D) {
-  return (static_cast<size_t>(p.tail) * 2 * kBM * p.n_split * D * sizeof(float) + 255) & ~size_t(255);
-}
-size_t tail_bytes(const TailPlan& p, int D) {
-  if (p.tail == 0) return 0;
-  return tail_o_bytes(p, D) + static_cast<size_t>(p.tail) * 2 * kBM * p.n_split * sizeof(float);
-}
-
-TailPlan plan_for(int B, int Hq, int Nq, int Nk, int sms) {
-  const long long units = static_cast<long long>((Nq + 2 * kBM - 1) / (2 * kBM)) * B * Hq;
-  return tail_plan(units, (Nk + kBN - 1) / kBN, sms);
-}
-
-template <Dt DT, int D, int MASK, bool ALIBI>
-cudaError_t launch_cfg(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-                       int Nq, int Nk, float scale, int window, const float* alibi, unsigned* status,
-                       const TailPlan& plan, void* ws, cudaStream_t s) {
-  alignas(64) CUtensorMap tq, tk, tv;
-  cudaError_t err = cudaSuccess;
-  if (!encode_tma_3d_16bit(&tq, q, D, Nq, uint64_t(B) * Hq, kBM, &err)) return err;
-  if (!encode_tma_3d_16bit(&tk, k, D, Nk, uint64_t(B) * Hkv, kBN, &err)) return err;
-  if (!encode_tma_3d_16bit(&tv, v, D, Nk, uint64_t(B) * Hkv, kBN, &err)) return err;
-  const int nqt = (Nq + 2 * kBM - 1) / (2 * kBM);
-  const long long grid = static_cast<long long>(nqt) * B * Hq;
-  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  const int smem = Cfg<D>::kTiles + 1024 + static_cast<int>(sizeof(TcBars)) + 64;
-  auto kern = attn_tc_kernel<DT, D, MASK, ALIBI>;
-  err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (err != cudaSuccess) return err;
-  const bool split = MASK == 0 && plan.tail > 0 && ws != nullptr;
-  float* o_part = split ? static_cast<float*>(ws) : nullptr;
-  float* lse_part = split ? reinterpret_cast<float*>(static_cast<char*>(ws) + tail_o_bytes(plan, D)) : nullptr;
-  const long long n_full = split ? plan.n_full : grid;
-  const long long ctas = split ? plan.n_full + static_cast<long long>(plan.tail) * plan.n_split : grid;
-  kern<<<static_cast<unsigned>(ctas), kThreads, smem, s>>>(tq, tk, tv, static_cast<uint16_t*>(o), lse, Hq, Hkv, Nq,
-                                                           Nk, B * Hq, nqt, scale * kLog2e, window, alibi, status,
-                                                           static_cast<int>(n_full), split ? plan.n_split : 1,
-                                                           o_part, lse_part);
-  err = cudaGetLastError();
-  if (err != cudaSuccess || !split) return err;
-  const int rows = plan.tail * 2 * kBM;
-  const AttnTailRows map{static_cast<int>(plan.n_full), B * Hq, nqt, Nq};
-  lse_merge_kernel<DT><<<(rows + kMergeWarps - 1) / kMergeWarps, kMergeWarps * 32, 0, s>>>(
-      o_part, lse_part, o, lse, rows, plan.n_split, D, map);
-  return cudaGetLastError();
-}
-
-template <Dt DT, int D>
-cudaError_t launch_d(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-                     int Nq, int Nk, float scale, int causal, int window, const float* alibi, unsigned* status,
-                     const TailPlan& plan, void* ws, cudaStream_t s) {
-  const TailPlan none{0, 0, 1};
-  if (!causal)
-    return launch_cfg<DT, D, 0, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, 0, nullptr, status, plan, ws, s);
-  if (window > 0) {
-    return alibi ? launch_cfg<DT, D, 2, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, window, alibi, status,
-                                              none, nullptr, s)
-                 : launch_cfg<DT, D, 2, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, window, nullptr, status,
-                                               none, nullptr, s);
-  }
-  return alibi ? launch_cfg<DT, D, 1, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, 0, alibi, status, none,
-                                            nullptr, s)
-               : launch_cfg<DT, D, 1, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, 0, nullptr, status, none,
-                                             nullptr, s);
-}
-
-}  // namespace
 
 size_t attn_tc_workspace_bytes(int B, int Hq, int Nq, int Nk, int D, int causal, int sms) {
   if (causal) return 0;
@@ -669,18 +12,18 @@ size_t attn_tc_workspace_bytes(int B, int Hq, int Nq, int Nk, int D, int causal,
 
 cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                            int Nq, int Nk, int D, float scale, int causal, int window, const float* alibi, Dt dt,
-                           unsigned* status, void* ws, int sms, cudaStream_t s) {
+                           unsigned* status, void* ws, int sms, int rope, double rope_base, int rope_pos,
+                           cudaStream_t s) {
+  if (rope != 0)
+    return launch_attn_tc_rope(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi, dt, status, ws,
+                               sms, rope, rope_base, rope_pos, s);
   // Windows of up to kWindowPersistMax keys leave units so short that the
   // persistent schedule of attn_fwd_tc_window.cu wins (measured at N = 4096:
   // W = 128 -18%, 256 -17%, 1024 -7% time; 2048 equal).
   if (causal && window > 0 && window <= kWindowPersistMax && D == 64)
     return launch_attn_tc_window(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, window, alibi, dt, status, sms, s);
-  const TailPlan plan = plan_for(B, Hq, Nq, Nk, sms);
-#define RF_ATTN_ARGS q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, alibi, status, plan, ws, s
-  if (dt == Dt::BF16) return D == 128 ? launch_d<Dt::BF16, 128>(RF_ATTN_ARGS) : launch_d<Dt::BF16, 64>(RF_ATTN_ARGS);
-  if (dt == Dt::F16) return D == 128 ? launch_d<Dt::F16, 128>(RF_ATTN_ARGS) : launch_d<Dt::F16, 64>(RF_ATTN_ARGS);
-#undef RF_ATTN_ARGS
-  return cudaErrorNotSupported;
+  return launch_rope_mode<0>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi, dt, status, ws, sms,
+                             AttnRope{}, s);
 }
 
 }  // namespace rf

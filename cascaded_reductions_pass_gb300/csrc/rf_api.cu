@@ -193,9 +193,16 @@ rf_status_t rf_device_status(void* stream, int clear) {
 
 namespace {
 
+struct RopeOpt {
+  int mode = 0;
+  float base = 0.f;
+  int pos = 0;
+};
+
 rf_status_t attn_impl(const char* name, const void* q, const void* k, const void* v, void* o, float* lse, int B,
                       int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal, int window,
-                      const float* alibi, void* ws, size_t ws_bytes, rf_dtype_t dtype, void* stream) {
+                      const float* alibi, void* ws, size_t ws_bytes, rf_dtype_t dtype, void* stream,
+                      const RopeOpt& rope = RopeOpt{}) {
   if (!q || !k || !v || !o) return fail(RF_ERR_INVALID_ARG, "%s: q, k, v and o must be non-null", name);
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || D <= 0)
     return fail(RF_ERR_INVALID_ARG, "%s: sizes must be positive (B=%d Hq=%d Hkv=%d Nq=%d Nk=%d D=%d)", name, B, Hq,
@@ -213,6 +220,17 @@ rf_status_t attn_impl(const char* name, const void* q, const void* k, const void
     return fail(RF_ERR_UNSUPPORTED, "%s: causal mask requires Nq == Nk (got %d, %d)", name, Nq, Nk);
   if (!causal && (window > 0 || alibi))
     return fail(RF_ERR_UNSUPPORTED, "%s: a sliding window and ALiBi need the causal mask", name);
+  if (rope.mode < 0 || rope.mode > 2) return fail(RF_ERR_INVALID_ARG, "%s: rope=%d must be 0, 1 or 2", name, rope.mode);
+  if (rope.mode) {
+    if (rope.pos < 0) return fail(RF_ERR_INVALID_ARG, "%s: rope_pos_offset must be >= 0", name);
+    if (!std::isfinite(rope.base) || rope.base < 0.0f || rope.base == 1.0f)
+      return fail(RF_ERR_INVALID_ARG, "%s: rope_base must be finite, positive and not 1 (0 = 10000)", name);
+    if (dtype == RF_F32)
+      return fail(RF_ERR_UNSUPPORTED, "%s: rotary embedding inside the kernel needs f16 or bf16", name);
+    if (alibi) return fail(RF_ERR_UNSUPPORTED, "%s: rotary embedding with ALiBi is not built", name);
+    if (static_cast<long long>(rope.pos) + (Nq > Nk ? Nq : Nk) > (1LL << 24))
+      return fail(RF_ERR_UNSUPPORTED, "%s: rotary positions reach past 2^24", name);
+  }
   if (dtype == RF_F32) {
     if (D % 4 != 0 || D > 128)
       return fail(RF_ERR_UNSUPPORTED, "%s: f32 path needs D %% 4 == 0 and D <= 128 (D=%d)", name, D);
@@ -234,7 +252,7 @@ rf_status_t attn_impl(const char* name, const void* q, const void* k, const void
     if (ws_bytes < need)
       return fail(RF_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", name, need, ws_bytes);
     RF_TRY(check_dev_ptr(ws, "workspace"));
-  } else if (dtype != RF_F32 && causal && window > 0 && window <= rf::kWindowPersistMax && D == 64) {
+  } else if (dtype != RF_F32 && causal && window > 0 && window <= rf::kWindowPersistMax && D == 64 && !rope.mode) {
     // the persistent windowed kernel
     sms = rf::device_sm_count();
   }
@@ -245,8 +263,10 @@ rf_status_t attn_impl(const char* name, const void* q, const void* k, const void
                     name);
   unsigned* st = rf::device_status_ptr();
   if (!st) return fail(RF_ERR_CUDA, "%s: cannot resolve the device status word", name);
+  const double rope_base = rope.base == 0.0f ? 10000.0 : static_cast<double>(rope.base);
   return launched(rf::launch_attn_tc(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi,
-                                     static_cast<rf::Dt>(dtype), st, sms > 0 ? ws : nullptr, sms, s),
+                                     static_cast<rf::Dt>(dtype), st, sms > 0 ? ws : nullptr, sms, rope.mode,
+                                     rope_base, rope.pos, s),
                   name);
 }
 
@@ -268,8 +288,14 @@ rf_status_t rf_attn_fwd_ex(const void* q, const void* k, const void* v, void* o,
   const float* alibi = opts ? opts->alibi_slopes : nullptr;
   void* ws = opts ? opts->workspace : nullptr;
   const size_t ws_bytes = opts ? opts->workspace_bytes : 0;
+  RopeOpt rope;
+  if (opts) {
+    rope.mode = opts->rope;
+    rope.base = opts->rope_base;
+    rope.pos = opts->rope_pos_offset;
+  }
   return attn_impl("rf_attn_fwd_ex", q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi, ws,
-                   ws_bytes, dtype, stream);
+                   ws_bytes, dtype, stream, rope);
 }
 
 size_t rf_attn_fwd_workspace_bytes(int B, int Hq, int Nq, int Nk, int D, int causal, rf_dtype_t dtype) {

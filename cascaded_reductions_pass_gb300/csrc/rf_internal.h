@@ -45,10 +45,17 @@ cudaError_t launch_decode_split(const void* q, const void* k, const void* v, flo
 // on `sms` SMs are split along the keys and merged; ws must then hold
 // attn_tc_workspace_bytes(...) bytes (0 when nothing is split).
 size_t attn_tc_workspace_bytes(int B, int Hq, int Nq, int Nk, int D, int causal, int sms);
+// rope: 0 none, 1 rotary embedding of the Q rows inside the kernel, 2 of the Q
+// and K rows (positions rope_pos + row, angles base^(-2i/D) with base rope_base).
 cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* o, float* lse,
                            int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal,
                            int window, const float* alibi, Dt dt, unsigned* status, void* ws, int sms,
-                           cudaStream_t s);
+                           int rope, double rope_base, int rope_pos, cudaStream_t s);
+// the rotary modes 1 and 2 of launch_attn_tc (attn_fwd_tc_rope.cu); no ALiBi
+cudaError_t launch_attn_tc_rope(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                                int Hkv, int Nq, int Nk, int D, float scale, int causal, int window,
+                                const float* alibi, Dt dt, unsigned* status, void* ws, int sms, int rope,
+                                double rope_base, int rope_pos, cudaStream_t s);
 
 // causal sliding-window attention at D = 64 for 16-bit inputs as a persistent
 // kernel, one CTA per SM walking a list of 256-row units (attn_fwd_tc_window.cu);

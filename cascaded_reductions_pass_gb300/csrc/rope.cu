@@ -13,26 +13,17 @@
 // issue slots that already bound the D = 64 kernel; one pass over Q and K
 // costs their bytes twice at HBM speed instead.
 //
-// Angles: the host passes base^(-2i/D) computed in double and split into two
-// floats (hi + lo).  The kernel forms p * (hi + lo) as a float pair (the
-// product's rounding error recovered with an FMA), reduces it modulo 2 pi by
-// Cody and Waite's method with 2 pi split into three floats, and calls
-// sincosf on the reduced angle, so positions in the tens of thousands keep
-// angle errors near 1e-7.  Each CTA builds a cos/sin table for its positions
-// in shared memory and reuses it across all (batch, head) rows.
+// Angles: see rope_angle.cuh (accurate p * base^(-2i/D), reduced modulo
+// 2 pi, then sincosf).  Each CTA builds a cos/sin table for its positions in
+// shared memory and reuses it across all (batch, head) rows.
 //
 // Work: a thread takes one pair of 16-byte chunks of a row (dims c*8..c*8+7
 // and the same dims + D/2), four pairs at a time so that eight loads are in
 // flight.  In place is allowed: each thread writes exactly what it read.
 #include "rf_device.cuh"
+#include "rope_angle.cuh"
 
 namespace rf {
-
-struct RopeParams {
-  float fhi[kRopeMaxHalf], flo[kRopeMaxHalf];  // base^(-2i/D) = fhi[i] + flo[i]
-  float two_pi[3];                             // 2 pi = sum of the three floats
-  float inv_two_pi;
-};
 
 namespace {
 
@@ -57,11 +48,7 @@ __device__ __forceinline__ uint4 rotate(const uint4& a, const uint4& b, const fl
   Pack<DT>::unpack(a, xa);
   Pack<DT>::unpack(b, xb);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const float2 t = cs[e * stride];  // (cos, sin)
-    ya[e] = fmaf(xa[e], t.x, -xb[e] * t.y);
-    yb[e] = fmaf(xa[e], t.y, xb[e] * t.x);
-  }
+  for (int e = 0; e < 8; ++e) rope_rotate(xa[e], xb[e], cs[e * stride], ya[e], yb[e]);
   b_out = Pack<DT>::pack(yb);
   return Pack<DT>::pack(ya);
 }
@@ -125,18 +112,7 @@ __global__ void __launch_bounds__(kThreads) rope_kernel(const uint4* __restrict_
   const int nb = min(kNB, N - n0);
   for (int e = threadIdx.x; e < kNB * H2; e += kThreads) {
     const int nl = e / H2, i = e - nl * H2;
-    // theta = p * (fhi + flo) as th + tl, then th + tl - j * 2 pi with j = nearest integer
-    const float p = static_cast<float>(pos_offset + n0 + nl);
-    const float th = p * prm.fhi[i];
-    const float tl = fmaf(p, prm.flo[i], fmaf(p, prm.fhi[i], -th));
-    const float j = rintf(th * prm.inv_two_pi);
-    float r = fmaf(-j, prm.two_pi[0], th);
-    r = fmaf(-j, prm.two_pi[1], r);
-    r = fmaf(-j, prm.two_pi[2], r);
-    r += tl;
-    float s, c;
-    sincosf(r, &s, &c);
-    cs[nl * RS + (i & 7) * CP + (i >> 3)] = make_float2(c, s);
+    cs[nl * RS + (i & 7) * CP + (i >> 3)] = rope_cs(static_cast<float>(pos_offset + n0 + nl), i, prm);
   }
   __syncthreads();
 
@@ -168,18 +144,7 @@ cudaError_t launch_dt(const void* q, const void* k, void* qo, void* ko, int BHq,
 
 cudaError_t launch_rope_qk(const void* q, const void* k, void* q_out, void* k_out, int BHq, int BHkv, int N, int D,
                            double base, int pos_offset, Dt dt, cudaStream_t s) {
-  RopeParams prm;
-  const int half = D / 2;
-  for (int i = 0; i < kRopeMaxHalf; ++i) {
-    const double f = i < half ? pow(base, -2.0 * i / D) : 0.0;
-    prm.fhi[i] = static_cast<float>(f);
-    prm.flo[i] = static_cast<float>(f - static_cast<double>(prm.fhi[i]));
-  }
-  const double two_pi = 2.0 * 3.14159265358979323846;
-  prm.two_pi[0] = static_cast<float>(two_pi);
-  prm.two_pi[1] = static_cast<float>(two_pi - static_cast<double>(prm.two_pi[0]));
-  prm.two_pi[2] = static_cast<float>(two_pi - static_cast<double>(prm.two_pi[0]) - static_cast<double>(prm.two_pi[1]));
-  prm.inv_two_pi = static_cast<float>(1.0 / two_pi);
+  const RopeParams prm = make_rope_params(base, D);
   switch (dt) {
     case Dt::F16: return launch_dt<Dt::F16>(q, k, q_out, k_out, BHq, BHkv, N, D, pos_offset, prm, s);
     case Dt::BF16: return launch_dt<Dt::BF16>(q, k, q_out, k_out, BHq, BHkv, N, D, pos_offset, prm, s);

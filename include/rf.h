@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define RF_VERSION 10000 /* 1.0.0 */
+#define RF_VERSION 10100 /* 1.1.0 */
 
 typedef enum {
   RF_OK = 0,
@@ -108,6 +108,21 @@ rf_status_t rf_attn_fwd(const void* q, const void* k, const void* v, void* o, fl
  *                 rf_attn_fwd_workspace_bytes(...) bytes; a null workspace
  *                 runs every unit whole (same results up to rounding order).
  *                 Calls that overlap on the GPU must not share a workspace.
+ *   rope          rotary position embedding fused into the load (AttnFuse,
+ *                 Figure 1 and Table 4): the pair (x_i, x_{i+D/2}) of a row at
+ *                 position p turns by p * rope_base^(-2i/D), with
+ *                 p = rope_pos_offset + row index.  1 turns the Q rows once per
+ *                 CTA after their load (for K already rotated, e.g. a cached
+ *                 K); 2 also turns the K rows of every key tile, which every
+ *                 CTA that streams the tile repeats.  q, k and v are not
+ *                 modified.  The result equals attention over the rows that
+ *                 rf_rope_qk writes (Q bit for bit; K up to the rounding of
+ *                 its angles' cosines and sines).  16-bit paths only, without
+ *                 ALiBi (RF_ERR_UNSUPPORTED otherwise); positions must stay
+ *                 below 2^24; rope outside {0, 1, 2}, a negative offset or a
+ *                 base that is negative, 1 or not finite is RF_ERR_INVALID_ARG.
+ *                 Callers should zero the whole struct before setting fields:
+ *                 versions before 1.1.0 do not have these three.
  * The window and ALiBi need the causal mask (RF_ERR_UNSUPPORTED otherwise).
  * The LSE output includes the ALiBi bias.  Everything else (layouts,
  * supported dtypes and head dims, errors) is as rf_attn_fwd; a negative window
@@ -119,6 +134,10 @@ typedef struct rf_attn_opts_t {
   const float* alibi_slopes;
   void* workspace;        /* nullable device memory, see rf_attn_fwd_workspace_bytes */
   size_t workspace_bytes;
+  /* since version 1.1.0: rotary embedding applied inside the kernel */
+  int rope;               /* 0 none, 1 rotate the Q rows, 2 rotate the Q and K rows */
+  float rope_base;        /* angle base; 0 means 10000 */
+  int rope_pos_offset;    /* position of query row 0 and of key 0 (>= 0) */
 } rf_attn_opts_t;
 rf_status_t rf_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
                            int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale,

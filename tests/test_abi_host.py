@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version(lib):
-    assert lib.rf_version() == 10000
+    assert lib.rf_version() == 10100  # 1.1.0: rotary embedding fields in rf_attn_opts_t
 
 
 P = ctypes.c_void_p(0x10000)  # aligned, never dereferenced: every case below fails a host check first
@@ -176,6 +176,25 @@ def test_attn_ex_rejects(lib):
     assert call(AttnOpts(0, 0, 0x10000)) == rf.RF_ERR_UNSUPPORTED
     assert call(AttnOpts(1, 16, None), Nk=9) == rf.RF_ERR_UNSUPPORTED and "Nq == Nk" in lib.rf_last_error().decode()
     assert call(AttnOpts(1, 16, 0x10002)) == rf.RF_ERR_INVALID_ARG and "aligned" in lib.rf_last_error().decode()
+
+
+def test_attn_ex_rejects_bad_rope_options(lib):
+    from cascaded_reductions_pass_gb300._binding import AttnOpts
+
+    def call(rope, base=0.0, pos=0, dtype=1, alibi=None, N=8):
+        opts = AttnOpts(1, 0, alibi, None, 0, rope, base, pos)
+        return lib.rf_attn_fwd_ex(P, P, P, P, None, 1, 2, 1, N, N, 64, 0.125, ctypes.byref(opts), dtype, S)
+
+    err = lambda: lib.rf_last_error().decode()
+    assert call(3) == rf.RF_ERR_INVALID_ARG and "rope" in err()
+    assert call(-1) == rf.RF_ERR_INVALID_ARG and "rope" in err()
+    assert call(1, pos=-5) == rf.RF_ERR_INVALID_ARG and "rope_pos_offset" in err()
+    assert call(2, base=1.0) == rf.RF_ERR_INVALID_ARG and "rope_base" in err()
+    assert call(2, base=-3.0) == rf.RF_ERR_INVALID_ARG and "rope_base" in err()
+    assert call(2, base=float("inf")) == rf.RF_ERR_INVALID_ARG and "rope_base" in err()
+    assert call(1, dtype=0) == rf.RF_ERR_UNSUPPORTED and "f16 or bf16" in err()
+    assert call(1, alibi=0x10000) == rf.RF_ERR_UNSUPPORTED and "ALiBi" in err()
+    assert call(2, pos=(1 << 24) - 4) == rf.RF_ERR_UNSUPPORTED and "2^24" in err()
 
 
 def test_ablation_workspace_bytes(lib):
