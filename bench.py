@@ -529,6 +529,45 @@ def measure_ablations(dev, steps, warmup, flush, peaks):
     return out
 
 
+def rope_crossover(dev, flush, steps=10, warmup=3):
+    """AttnFuse's "Rotation Calculus" question (Table 4) on this GPU: causal
+    attention over rotary-embedded Q and K, with the rotation done
+    (a) by the separate pass over Q and K, then attention;
+    (b) by the separate pass over K only, Q turned inside the attention kernel;
+    (c) inside the attention kernel for both Q and K;
+    against (0) the same attention without rotation, for a range of N.
+    Returns one row per shape with each variant's mean step time (ms)."""
+    import cascaded_reductions_pass_gb300 as rf
+
+    rows = []
+    for B, H, D, dtype in ((4, 12, 64, "f16"), (2, 16, 128, "bf16")):
+        for N in (1024, 2048, 4096, 8192, 16384):
+            q, k, v = (t.to(dev) for t in inputs.attn_inputs(B, H, H, N, N, D, dtype, seed=N + D))
+            scale = float(np.float32(1.0 / math.sqrt(D)))
+            qo, ko, o = torch.empty_like(q), torch.empty_like(k), torch.empty_like(q)
+            lse = torch.empty(B, H, N, dtype=torch.float32, device=dev)
+
+            def attn(qq, kk, mode):
+                rf.rf_attn_fwd_ex(qq, kk, v, o, lse, scale=scale, causal=True, rope=mode)
+
+            variants = {
+                "attention, no rotation": lambda: attn(q, k, 0),
+                "separate pass (Q, K) + attention": lambda: (rf.rf_rope_qk(q, k, qo, ko), attn(qo, ko, 0)),
+                "separate pass (K) + Q in kernel": lambda: (rf.rf_rope_qk(k, None, ko), attn(q, ko, 1)),
+                "Q and K in kernel": lambda: attn(q, k, 2),
+            }
+            res = {}
+            for name, fn in variants.items():
+                class _S:
+                    step = staticmethod(fn)
+
+                res[name] = float(np.mean(time_steps(_S(), steps, warmup, flush)))
+            rows.append({"B": B, "H": H, "N": N, "D": D, "dtype": dtype, "ms": res})
+            del q, k, v, qo, ko, o, lse
+            torch.cuda.empty_cache()
+    return rows
+
+
 # The five workload configurations of the headline metric, in their order, then the other workloads.
 CONFIG_ORDER = ["attn_tiny_f32", "attn_fwd_f16_d64", "attn_fwd_causal_gqa_bf16_d128", "decode_splitkv_bf16",
                 "layernorm_residual_bf16"]
@@ -586,6 +625,8 @@ def main():
     ap.add_argument("--no-parts", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    ap.add_argument("--rope-crossover", action="store_true",
+                    help="only time rotary causal attention three ways over N (AttnFuse's Rotation Calculus)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override B (attention, decode) or rows (LayerNorm): a smaller case for profiler captures")
     args = ap.parse_args()
@@ -629,6 +670,11 @@ def main():
     rf.load()
     peaks = load_peaks()
     flush = L2Flush(dev)
+    if args.rope_crossover:
+        if rank == 0:
+            print(json.dumps({"rope_crossover": rope_crossover(dev, flush),
+                              "l2_flush": "before every step, outside the events", "steps": 10, "warmup": 3}))
+        return
     sampler = ClockSampler(local)
     sampler.start()
 

@@ -14,7 +14,7 @@
 // costs their bytes twice at HBM speed instead.
 //
 // Angles: see rope_angle.cuh (accurate p * base^(-2i/D), reduced modulo
-// 2 pi, then sincosf).  Each CTA builds a cos/sin table for its positions in
+// 2 pi, then the hardware sine and cosine on the reduced angle).  Each CTA builds a cos/sin table for its positions in
 // shared memory and reuses it across all (batch, head) rows.
 //
 // Work: a thread takes one pair of 16-byte chunks of a row (dims c*8..c*8+7

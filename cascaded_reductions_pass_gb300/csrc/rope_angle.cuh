@@ -7,10 +7,14 @@
 //
 // The host passes base^(-2i/D) computed in double and split into two floats
 // (hi + lo).  The device forms p * (hi + lo) as a float pair (the product's
-// rounding error recovered with an FMA), reduces it modulo 2 pi by Cody and
-// Waite's method with 2 pi split into three floats, and calls sincosf on the
-// reduced angle, so positions in the tens of thousands keep angle errors near
-// 1e-7.
+// rounding error recovered with an FMA) and reduces it modulo 2 pi by Cody and
+// Waite's method with 2 pi split into three floats, so positions in the tens
+// of thousands keep angle errors near 1e-7.  The reduced angle lies in
+// [-pi, pi], where the hardware sine and cosine (__sincosf) are accurate to a
+// few 1e-7 absolute; their error therefore does not grow with the position.
+// (The library sincosf costs several times more per angle, which at one angle
+// per element pair made the rotation inside the attention kernel cost more
+// than a separate pass over Q and K.)
 #pragma once
 
 #include <math.h>
@@ -52,7 +56,7 @@ __device__ __forceinline__ float2 rope_cs(float p, int i, const RopeParams& prm)
   r = fmaf(-j, prm.two_pi[2], r);
   r += tl;
   float s, c;
-  sincosf(r, &s, &c);
+  __sincosf(r, &s, &c);
   return make_float2(c, s);
 }
 

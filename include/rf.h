@@ -332,7 +332,9 @@ rf_status_t rf_softmax_xent(const void* logits, const long long* targets, float*
  *   k      [B, Hkv, N, D] dtype (read)        k_out  [B, Hkv, N, D] (written)
  * k and k_out are both null (rotate Q only) or both non-null.  An output may
  * be its own input (in place).  Angles are formed to about 1e-7 rad for any
- * position below 2^24.
+ * position below 2^24 and reduced to [-pi, pi]; their cosines and sines come
+ * from the hardware functions, accurate to a few 1e-7 there.  The rotation
+ * inside rf_attn_fwd_ex (rope = 1) uses the same function, bit for bit.
  *
  * Supported: dtype RF_F16 / RF_BF16; D in {64, 128, 256}; base > 0, finite,
  * not 1; pos_offset >= 0 and pos_offset + N <= 2^24; pointers 16-byte aligned.
