@@ -23,8 +23,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "librf.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "rf.h")
 
-RF_OK, RF_ERR_INVALID_ARG, RF_ERR_UNSUPPORTED, RF_ERR_CUDA, RF_ERR_TIMEOUT = range(5)
-STATUS_NAMES = {0: "RF_OK", 1: "RF_ERR_INVALID_ARG", 2: "RF_ERR_UNSUPPORTED", 3: "RF_ERR_CUDA", 4: "RF_ERR_TIMEOUT"}
+RF_OK, RF_ERR_INVALID_ARG, RF_ERR_UNSUPPORTED, RF_ERR_CUDA, RF_ERR_TIMEOUT, RF_ERR_CHECK = range(6)
+STATUS_NAMES = {0: "RF_OK", 1: "RF_ERR_INVALID_ARG", 2: "RF_ERR_UNSUPPORTED", 3: "RF_ERR_CUDA", 4: "RF_ERR_TIMEOUT",
+                5: "RF_ERR_CHECK"}
 DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
 _lib = None
@@ -53,6 +54,8 @@ _SIGNATURES = {
     "rf_version": ([], _i),
     "rf_device_status": ([_vp, _i], _i),
     "rf_selftest_wait_timeout": ([ctypes.c_uint, _vp], _i),
+    "rf_selftest_check": ([_vp], _i),
+    "rf_checks_enabled": ([], _i),
     "rf_ablation_workspace_bytes": ([_i, _i, _i, _i, _i], _sz),
     "rf_rope_qk": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp], _i),
     "rf_layernorm_ablation": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _f, _i, _vp, _sz, _i, _vp], _i),
@@ -134,13 +137,23 @@ def rf_last_error() -> str:
 
 
 def rf_device_status(stream=None, clear=True) -> int:
-    """Synchronise the stream and return the device status (RF_OK or RF_ERR_TIMEOUT)."""
+    """Synchronise the stream and return the device status (RF_OK, RF_ERR_CHECK or RF_ERR_TIMEOUT)."""
     return load().rf_device_status(_stream(stream), int(bool(clear)))
 
 
 def rf_selftest_wait_timeout(timeout_us=2000, stream=None):
     """Launch the bounded-wait self-test (a wait that is meant to run out)."""
     _check(load().rf_selftest_wait_timeout(int(timeout_us), _stream(stream)))
+
+
+def rf_selftest_check(stream=None):
+    """Launch the index-check self-test (a check that always fails, no memory access)."""
+    _check(load().rf_selftest_check(_stream(stream)))
+
+
+def rf_checks_enabled() -> bool:
+    """True for a library built with -DRF_CHECKS (every kernel checks its indices)."""
+    return bool(load().rf_checks_enabled())
 
 
 def rf_attn_fwd(q, k, v, o, lse=None, scale=None, causal=False, stream=None):
@@ -438,12 +451,13 @@ def ablation_workspace(op, variant, rows, cols, dtype, device="cuda"):
 
 __all__ = [
     "RFError", "load", "declared_symbols", "rf_version", "rf_last_error", "rf_device_status",
-    "rf_selftest_wait_timeout", "rf_attn_fwd",
+    "rf_selftest_wait_timeout", "rf_selftest_check", "rf_checks_enabled", "rf_attn_fwd",
     "rf_attn_fwd_ex", "AttnOpts", "alibi_slopes", "rf_attn_fwd_workspace_bytes", "attn_workspace",
     "rf_attn_decode_splitkv_workspace_bytes", "rf_attn_decode_splitkv", "rf_attn_decode_splitkv_noalloc",
     "rf_lse_merge", "rf_layernorm_fused", "rf_rmsnorm_fused", "rmsnorm", "rf_softmax_xent", "softmax_xent",
     "attention", "decode", "decode_workspace", "decode_partials_view", "layernorm",
     "rf_ablation_workspace_bytes", "rf_layernorm_ablation", "rf_softmax_xent_ablation", "ablation_workspace",
     "LN_VARIANTS", "XENT_VARIANTS", "rf_rope_qk",
-    "RF_OK", "RF_ERR_INVALID_ARG", "RF_ERR_UNSUPPORTED", "RF_ERR_CUDA", "RF_ERR_TIMEOUT",
+    "RF_OK", "RF_ERR_INVALID_ARG", "RF_ERR_UNSUPPORTED", "RF_ERR_CUDA", "RF_ERR_TIMEOUT", "RF_ERR_CHECK",
+    "STATUS_NAMES",
 ]

@@ -48,18 +48,36 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(p) <= t for p in sources() + _headers() + [__file__])
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile every kernel for sm_103a and link librf.so; returns its path."""
+CHECKED_LIB = os.path.join(LIBDIR, "librf_checks.so")
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=(), checks: bool = False) -> str:
+    """Compile every kernel for sm_103a and link librf.so; returns its path.
+
+    checks=True builds the index-checked library instead (-DRF_CHECKS, its own
+    objects under _build/checks, linked as _lib/librf_checks.so): every kernel
+    then checks the indices it computes and records RF_ERR_CHECK instead of
+    making an access that falls outside its buffer."""
+    if checks:
+        return _build_into(os.path.join(OBJDIR, "checks"), CHECKED_LIB, ("-DRF_CHECKS", *extra_flags), force, verbose)
     if not force and not extra_flags and up_to_date():
         return LIB
+    return _build_into(OBJDIR, LIB, tuple(extra_flags), force, verbose)
+
+
+def _build_into(objdir, lib, extra_flags, force, verbose) -> str:
+    """Compile every source into objdir and link `lib`.  Objects newer than
+    their source and every header are reused, except in the default object
+    directory when extra flags are given (those objects were built without)."""
     nvcc = _nvcc()
-    os.makedirs(OBJDIR, exist_ok=True)
+    os.makedirs(objdir, exist_ok=True)
     os.makedirs(LIBDIR, exist_ok=True)
+    reuse = not force and (not extra_flags or objdir != OBJDIR)
     hdr_time = max([os.path.getmtime(p) for p in _headers()] + [os.path.getmtime(__file__)])
 
     def compile_one(src):
-        obj = os.path.join(OBJDIR, os.path.basename(src)[:-3] + ".o")
-        if (not force and not extra_flags and os.path.exists(obj)
+        obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
+        if (reuse and os.path.exists(obj)
                 and os.path.getmtime(obj) >= max(os.path.getmtime(src), hdr_time)):
             return obj
         cmd = [nvcc, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
@@ -72,14 +90,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with concurrent.futures.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
            "-Xlinker", "-rpath,/usr/local/cuda/lib64"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link of librf.so failed:\n{res.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

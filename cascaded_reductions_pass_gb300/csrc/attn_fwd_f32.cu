@@ -33,7 +33,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const float* __re
                                                                const float* __restrict__ v, float* __restrict__ o,
                                                                float* __restrict__ lse, int Hq, int Hkv, int Nq,
                                                                int Nk, int D, float scale, int causal, int window,
-                                                               const float* __restrict__ alibi) {
+                                                               const float* __restrict__ alibi, unsigned* status) {
   extern __shared__ float4 smem4[];
   float* smem = reinterpret_cast<float*>(smem4);
   const int KS = D + 4;               // padded K row stride (floats)
@@ -44,6 +44,8 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const float* __re
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.z, h = blockIdx.y, hk = h / (Hq / Hkv);
   const int q0 = blockIdx.x * kBM;
+  // the grid is (query blocks, Hq, B): a block past them has nothing to do
+  if (!RF_INB(q0 < Nq && h < Hq && hk < Hkv && D <= 32 * DC, status)) return;
   const float* qh = q + (static_cast<long long>(b) * Hq + h) * Nq * D;
   const float* kh = k + (static_cast<long long>(b) * Hkv + hk) * Nk * D;
   const float* vh = v + (static_cast<long long>(b) * Hkv + hk) * Nk * D;
@@ -141,16 +143,16 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const float* __re
 
 cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B, int Hq,
                             int Hkv, int Nq, int Nk, int D, float scale, int causal, int window, const float* alibi,
-                            cudaStream_t s) {
+                            unsigned* status, cudaStream_t s) {
   const dim3 grid((Nq + kBM - 1) / kBM, Hq, B);
   if (B > 65535 || Hq > 65535) return cudaErrorInvalidConfiguration;
   const size_t smem = sizeof(float) * (kBM * D + kBN * (D + 4) + kBN * D);
   const int dc = (D + 31) / 32;
   switch (dc) {
-    case 1: attn_f32_kernel<1><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi); break;
-    case 2: attn_f32_kernel<2><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi); break;
-    case 3: attn_f32_kernel<3><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi); break;
-    default: attn_f32_kernel<4><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi); break;
+    case 1: attn_f32_kernel<1><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi, status); break;
+    case 2: attn_f32_kernel<2><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi, status); break;
+    case 3: attn_f32_kernel<3><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi, status); break;
+    default: attn_f32_kernel<4><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi, status); break;
   }
   return cudaGetLastError();
 }

@@ -142,6 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool kSpec = D == 64 && MASK == 0 && !ALIBI;
   using C = Cfg<D>;
   constexpr int S = C::kStages;
+  static_assert(C::kOCol + 2 * D <= kTmemCols && (!C::kSepP || C::kPCol + kBN <= kTmemCols),
+                "TMEM columns of S, O and P must fit the allocation");
   constexpr bool kBF16 = DT == Dt::BF16;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -217,6 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
+      if (lane == 0) (void)RF_INB(bh < BH && r0 < Nq && kv_plane < (BH / Hq) * Hkv && lo0 >= 0 && nt1 <= n_kv, status);
       mbar_expect_tx_elect(&bars->q_full, 2 * C::kQBytes);
 #pragma unroll
       for (int t = 0; t < 2; ++t)
@@ -227,6 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int jj = 0; jj < n_load; ++jj) {  // ring slot jj holds key tile lo0 + jj
         const int st = jj % S, key0 = (lo0 + jj) * kBN;
+        if (lane == 0) (void)RF_INB(key0 < Nk, status);
         if (jj >= S && !(ok = mbar_wait_warp(&bars->k_empty[st], ((jj / S) - 1) & 1))) break;
         mbar_expect_tx_elect(&bars->k_full[st], C::kSepP ? 2 * C::kKVBytes : C::kKVBytes);
 #pragma unroll
@@ -416,6 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (!(ok = mbar_wait_warp(&bars->k_full[st], (jj / S) & 1))) break;
+        (void)RF_INB(st < S && w2 >= 0 && w2 < 2, status);
         uint8_t* tile = sK + st * C::kKVBytes;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -471,6 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = warp_wait(&bars->q_full, 0);
       if (ok) {
         const int rl = qw * 32 + lane;  // row within the tile
+        (void)RF_INB(rl < kBM && t < 2, status);
         uint8_t* qrow = sQ + t * C::kQBytes + rl * 128;
         const float p = static_cast<float>(rope_pos + row);
 #pragma unroll
@@ -643,13 +649,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = row < Nq;
       if (piece) {  // partial row g of the split tail: O_s and lse_s in fp32
         const long long g = static_cast<long long>(unit - n_full) * (2 * kBM) + (row - r0);
+        // the tail holds (gridDim.x - n_full) / n_split units of 2 * kBM partial rows
+        const bool in_ws = RF_INB(g < static_cast<long long>(gridDim.x - n_full) / n_split * (2 * kBM) &&
+                                      split < n_split, status);
         float4* prow = reinterpret_cast<float4*>(o_part + (g * n_split + split) * D);
 #pragma unroll
         for (int i = 0; i < D / 32; ++i) {
           uint32_t ov[32];
           tc_ld32(tO + 32 * i, ov);
           tc_wait_ld();
-          if (row_ok) {
+          if (row_ok && in_ws) {
 #pragma unroll
             for (int v4 = 0; v4 < 8; ++v4)
               prow[i * 8 + v4] =
@@ -657,8 +666,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                               __uint_as_float(ov[4 * v4 + 2]) * inv, __uint_as_float(ov[4 * v4 + 3]) * inv);
           }
         }
-        if (row_ok) lse_part[g * n_split + split] = (m_run + log2f(l_run)) * kLn2;
+        if (row_ok && in_ws) lse_part[g * n_split + split] = (m_run + log2f(l_run)) * kLn2;
       } else {
+        const bool in_o = RF_INB(bh < BH && (!row_ok || (row >= 0 && row < Nq)), status);
         uint4* orow =
             reinterpret_cast<uint4*>(o + (static_cast<long long>(bh) * Nq + (row_ok ? row : 0)) * D);
 #pragma unroll
@@ -670,20 +680,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e)
             pk[e] = Pack<DT>::pack2(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
-          if (row_ok) {
+          if (row_ok && in_o) {
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4)
               orow[i * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
           }
         }
-        if (row_ok && lse) lse[static_cast<long long>(bh) * Nq + row] = (m_run + log2f(l_run)) * kLn2;
+        if (row_ok && in_o && lse) lse[static_cast<long long>(bh) * Nq + row] = (m_run + log2f(l_run)) * kLn2;
       }
     } else if (!ok) {
       if (lane == 0) atomicOr(status, kStatusTimeout);
       bars->abort = 1;
       if (piece && row < Nq) {  // a split-tail piece marks its partial row invalid for the merge
         const long long g = static_cast<long long>(unit - n_full) * (2 * kBM) + (row - r0);
-        lse_part[g * n_split + split] = NAN;
+        if (RF_INB(g < static_cast<long long>(gridDim.x - n_full) / n_split * (2 * kBM), status))
+          lse_part[g * n_split + split] = NAN;
       }
     }
   }
@@ -764,7 +775,7 @@ cudaError_t launch_cfg(const void* q, const void* k, const void* v, void* o, flo
   const int rows = plan.tail * 2 * kBM;
   const AttnTailRows map{static_cast<int>(plan.n_full), B * Hq, nqt, Nq};
   lse_merge_kernel<DT><<<(rows + kMergeWarps - 1) / kMergeWarps, kMergeWarps * 32, 0, s>>>(
-      o_part, lse_part, o, lse, rows, plan.n_split, D, map);
+      o_part, lse_part, o, lse, rows, plan.n_split, D, map, static_cast<long long>(B) * Hq * Nq, status);
   return cudaGetLastError();
 }
 

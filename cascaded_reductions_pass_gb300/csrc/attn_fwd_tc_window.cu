@@ -159,6 +159,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it.bh < 0 || aborted(bars)) break;
         const int qb = k & 1;
         const int kv_plane = (it.bh / Hq) * Hkv + (it.bh % Hq) / (Hq / Hkv);
+        if (lane == 0)
+          (void)RF_INB(it.bh < sc.BH && it.r0 < Nq && it.lo0 >= 0 && it.nt1 * kBN < sc.Nk + kBN &&
+                           kv_plane < (sc.BH / Hq) * Hkv, status);
         if (k >= 2 && !(ok = mbar_wait_warp(&bars->q_empty[0][qb], ((k >> 1) - 1) & 1) &&
                              mbar_wait_warp(&bars->q_empty[1][qb], ((k >> 1) - 1) & 1)))
           break;
@@ -439,6 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv = 1.0f / l_run;
       const bool row_ok = row < Nq;
+      const bool in_o = RF_INB(bh < sc.BH && row >= 0, status);
       uint4* orow = reinterpret_cast<uint4*>(o + (static_cast<long long>(bh) * Nq + (row_ok ? row : 0)) * kWD);
 #pragma unroll
       for (int i = 0; i < kWD / 32; ++i) {
@@ -449,13 +453,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           pk[e] = Pack<DT>::pack2(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
-        if (row_ok) {
+        if (row_ok && in_o) {
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
             orow[i * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
         }
       }
-      if (row_ok && lse) lse[static_cast<long long>(bh) * Nq + row] = (m_run + log2f(l_run)) * kLn2;
+      if (row_ok && in_o && lse) lse[static_cast<long long>(bh) * Nq + row] = (m_run + log2f(l_run)) * kLn2;
       // O_t has been read (tcgen05.ld waited); the fence before this thread's
       // next p_ready arrival lets the next item's first PV_t overwrite it
     }

@@ -140,6 +140,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         uint8_t* dst = smem + st * kStageBytes;
         mbar_expect_tx(&bars->full[st], kStageBytes);
         const int key0 = static_cast<int>(lo) + it * kBN;
+        (void)RF_INB(key0 < L && plane < static_cast<int>(gridDim.z) * Hkv, status);
 #pragma unroll
         for (int bx = 0; bx < kBoxes; ++bx) {
           tma_load_3d(dst + bx * (kBN * 128), &tk, &bars->full[st], bx * 64, key0, plane);
@@ -158,10 +159,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint32_t qf[kDC][2];
     const int hq = hk * G + g;
     const uint32_t* qrow = reinterpret_cast<const uint32_t*>(q + (static_cast<long long>(b) * Hq + hq) * D);
+    const bool q_in = g >= G || RF_INB(b < static_cast<int>(gridDim.z) && hq < Hq, status);
 #pragma unroll
     for (int c = 0; c < kDC; ++c) {
-      qf[c][0] = g < G ? __ldg(qrow + 8 * c + t) : 0u;
-      qf[c][1] = g < G ? __ldg(qrow + 8 * c + 4 + t) : 0u;
+      qf[c][0] = g < G && q_in ? __ldg(qrow + 8 * c + t) : 0u;
+      qf[c][1] = g < G && q_in ? __ldg(qrow + 8 * c + 4 + t) : 0u;
     }
     const uint32_t smem_base = smem_u32(smem);
     // ldmatrix lane roles: K (non-transposed A) and V (transposed A) address maps.
@@ -265,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
       const int h = idx / D, d = idx - h * D;
       const long long row = static_cast<long long>(b) * Hq + hk * G + h;
+      if (!RF_INB(row < static_cast<long long>(gridDim.z) * Hq && split < S, status)) continue;
       o_part[(row * S + split) * D + d] = NAN;
       if (d == 0) lse_part[row * S + split] = NAN;
     }
@@ -288,6 +291,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       out = num / den;
       lse = (M + log2f(den)) * kLn2;
     }
+    if (!RF_INB(row < static_cast<long long>(gridDim.z) * Hq && split < S, status)) continue;
     o_part[(row * S + split) * D + d] = out;
     if (d == 0) lse_part[row * S + split] = lse;
   }

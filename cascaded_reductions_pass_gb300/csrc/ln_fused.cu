@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(1024) ln_fused_kernel(const uint4* __restrict_
                                                         const uint4* __restrict__ gamma,
                                                         const uint4* __restrict__ beta, uint4* __restrict__ out,
                                                         uint4* __restrict__ r_out, int rows, int nvec, int tpr,
-                                                        float inv_cols, float eps) {
+                                                        float inv_cols, float eps, unsigned* status) {
   using V = Vec2<DT>;
   constexpr int P = V::P;
   __shared__ float2 s_warp[32];
@@ -129,7 +129,8 @@ __global__ void __launch_bounds__(1024) ln_fused_kernel(const uint4* __restrict_
   const int slot = threadIdx.x / tpr;
   const int t = threadIdx.x - slot * tpr;
   const long long row = static_cast<long long>(blockIdx.x) * rows_per_cta + slot;
-  const bool row_ok = row < rows;
+  // the row's vectors t, t + tpr, ... must cover [0, nvec) within the tensor
+  const bool row_ok = row < rows && RF_INB(t < tpr && VPT * tpr >= nvec && slot < rows_per_cta, status);
   const long long base = row * nvec;
 
   // Issue every load of this thread's slice of the row before using any.
@@ -285,7 +286,7 @@ template <Dt DT, int VPT>
 __global__ void __launch_bounds__(1024) rms_fused_kernel(const uint4* __restrict__ x, const uint4* __restrict__ r,
                                                          const uint4* __restrict__ gamma, uint4* __restrict__ out,
                                                          uint4* __restrict__ r_out, int rows, int nvec, int tpr,
-                                                         float inv_cols, float eps) {
+                                                         float inv_cols, float eps, unsigned* status) {
   using V = Vec2<DT>;
   constexpr int P = V::P;
   __shared__ float s_warp[32];
@@ -294,7 +295,8 @@ __global__ void __launch_bounds__(1024) rms_fused_kernel(const uint4* __restrict
   const int slot = threadIdx.x / tpr;
   const int t = threadIdx.x - slot * tpr;
   const long long row = static_cast<long long>(blockIdx.x) * rows_per_cta + slot;
-  const bool row_ok = row < rows;
+  // the row's vectors t, t + tpr, ... must cover [0, nvec) within the tensor
+  const bool row_ok = row < rows && RF_INB(t < tpr && VPT * tpr >= nvec && slot < rows_per_cta, status);
   const long long base = row * nvec;
 
   uint4 xv[VPT], rv[VPT];
@@ -356,7 +358,7 @@ __global__ void __launch_bounds__(1024) rms_fused_kernel(const uint4* __restrict
 
 template <Dt DT, bool RMS>
 cudaError_t launch_dt(const void* x, const void* r, const void* g, const void* b, void* out, void* r_out,
-                      int rows, int cols, float eps, cudaStream_t s) {
+                      int rows, int cols, float eps, unsigned* status, cudaStream_t s) {
   constexpr int E = 2 * Vec2<DT>::P;
   const int nvec = cols / E;
   const int vpt = nvec >= 128 ? 4 : (nvec >= 64 ? 2 : 1);  // one warp per row from 128 vectors up
@@ -376,13 +378,13 @@ cudaError_t launch_dt(const void* x, const void* r, const void* g, const void* b
   const unsigned gr = static_cast<unsigned>(grid);
   if constexpr (RMS) {
     if (vpt == 4)
-      rms_fused_kernel<DT, 4><<<gr, threads, 0, s>>>(X, R, G, O, RO, rows, nvec, tpr, inv_cols, eps);
+      rms_fused_kernel<DT, 4><<<gr, threads, 0, s>>>(X, R, G, O, RO, rows, nvec, tpr, inv_cols, eps, status);
     else if (vpt == 2)
-      rms_fused_kernel<DT, 2><<<gr, threads, 0, s>>>(X, R, G, O, RO, rows, nvec, tpr, inv_cols, eps);
+      rms_fused_kernel<DT, 2><<<gr, threads, 0, s>>>(X, R, G, O, RO, rows, nvec, tpr, inv_cols, eps, status);
     else
-      rms_fused_kernel<DT, 1><<<gr, threads, 0, s>>>(X, R, G, O, RO, rows, nvec, tpr, inv_cols, eps);
+      rms_fused_kernel<DT, 1><<<gr, threads, 0, s>>>(X, R, G, O, RO, rows, nvec, tpr, inv_cols, eps, status);
   } else {
-#define RF_LN(V_, RO_) ln_fused_kernel<DT, V_, RO_><<<gr, threads, 0, s>>>(X, R, G, Bt, O, RO, rows, nvec, tpr, inv_cols, eps)
+#define RF_LN(V_, RO_) ln_fused_kernel<DT, V_, RO_><<<gr, threads, 0, s>>>(X, R, G, Bt, O, RO, rows, nvec, tpr, inv_cols, eps, status)
     if (RO) {
       if (vpt == 4) RF_LN(4, true); else if (vpt == 2) RF_LN(2, true); else RF_LN(1, true);
     } else {
@@ -399,21 +401,21 @@ cudaError_t launch_dt(const void* x, const void* r, const void* g, const void* b
 int layernorm_max_cols(Dt dt) { return 1024 * 4 * (dt == Dt::F32 ? 4 : 8); }
 
 cudaError_t launch_layernorm(const void* x, const void* r, const void* gamma, const void* beta, void* out,
-                             void* r_out, int rows, int cols, float eps, Dt dt, cudaStream_t s) {
+                             void* r_out, int rows, int cols, float eps, Dt dt, unsigned* status, cudaStream_t s) {
   switch (dt) {
-    case Dt::F32: return launch_dt<Dt::F32, false>(x, r, gamma, beta, out, r_out, rows, cols, eps, s);
-    case Dt::F16: return launch_dt<Dt::F16, false>(x, r, gamma, beta, out, r_out, rows, cols, eps, s);
-    case Dt::BF16: return launch_dt<Dt::BF16, false>(x, r, gamma, beta, out, r_out, rows, cols, eps, s);
+    case Dt::F32: return launch_dt<Dt::F32, false>(x, r, gamma, beta, out, r_out, rows, cols, eps, status, s);
+    case Dt::F16: return launch_dt<Dt::F16, false>(x, r, gamma, beta, out, r_out, rows, cols, eps, status, s);
+    case Dt::BF16: return launch_dt<Dt::BF16, false>(x, r, gamma, beta, out, r_out, rows, cols, eps, status, s);
   }
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_rmsnorm(const void* x, const void* r, const void* gamma, void* out, void* r_out, int rows, int cols,
-                           float eps, Dt dt, cudaStream_t s) {
+                           float eps, Dt dt, unsigned* status, cudaStream_t s) {
   switch (dt) {
-    case Dt::F32: return launch_dt<Dt::F32, true>(x, r, gamma, nullptr, out, r_out, rows, cols, eps, s);
-    case Dt::F16: return launch_dt<Dt::F16, true>(x, r, gamma, nullptr, out, r_out, rows, cols, eps, s);
-    case Dt::BF16: return launch_dt<Dt::BF16, true>(x, r, gamma, nullptr, out, r_out, rows, cols, eps, s);
+    case Dt::F32: return launch_dt<Dt::F32, true>(x, r, gamma, nullptr, out, r_out, rows, cols, eps, status, s);
+    case Dt::F16: return launch_dt<Dt::F16, true>(x, r, gamma, nullptr, out, r_out, rows, cols, eps, status, s);
+    case Dt::BF16: return launch_dt<Dt::BF16, true>(x, r, gamma, nullptr, out, r_out, rows, cols, eps, status, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -59,13 +59,14 @@ template <Dt DT, class RowMap>
 __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const float* __restrict__ o_part,
                                                                      const float* __restrict__ lse_part,
                                                                      void* __restrict__ o, float* __restrict__ lse,
-                                                                     int rows, int S, int D, RowMap out_row) {
+                                                                     int rows, int S, int D, RowMap out_row,
+                                                                     long long out_rows, unsigned* status) {
   __shared__ float s_w[kMergeWarps][kMergeMaxSplits];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long row = static_cast<long long>(blockIdx.x) * kMergeWarps + warp;
   if (row >= rows) return;
   const long long orow = out_row(row);  // where this row's result goes (< 0: nowhere)
-  if (orow < 0) return;
+  if (orow < 0 || !RF_INB(orow < out_rows && S <= kMergeMaxSplits, status)) return;
   const float* lp = lse_part + row * S;
 
   float mx = -INFINITY;

@@ -167,6 +167,14 @@ const char* rf_last_error(void) { return g_last_error; }
 
 int rf_version(void) { return RF_VERSION; }
 
+int rf_checks_enabled(void) {
+#ifdef RF_CHECKS
+  return 1;
+#else
+  return 0;
+#endif
+}
+
 rf_status_t rf_device_status(void* stream, int clear) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(s);
@@ -184,6 +192,7 @@ rf_status_t rf_device_status(void* stream, int clear) {
     cudaGetLastError();
     return fail(RF_ERR_CUDA, "status word access failed: %s", cudaGetErrorString(e));
   }
+  if (v & 2u) return fail(RF_ERR_CHECK, "a device-side index check failed (code 0x%x)", v);
   if (v != 0) return fail(RF_ERR_TIMEOUT, "a device-side bounded wait ran out (code 0x%x)", v);
   g_last_error[0] = '\0';
   return RF_OK;
@@ -256,13 +265,13 @@ rf_status_t attn_impl(const char* name, const void* q, const void* k, const void
     // the persistent windowed kernel
     sms = rf::device_sm_count();
   }
+  unsigned* st = rf::device_status_ptr();
+  if (!st) return fail(RF_ERR_CUDA, "%s: cannot resolve the device status word", name);
   if (dtype == RF_F32)
     return launched(rf::launch_attn_f32(static_cast<const float*>(q), static_cast<const float*>(k),
                                         static_cast<const float*>(v), static_cast<float*>(o), lse, B, Hq, Hkv, Nq, Nk,
-                                        D, scale, causal, window, alibi, s),
+                                        D, scale, causal, window, alibi, st, s),
                     name);
-  unsigned* st = rf::device_status_ptr();
-  if (!st) return fail(RF_ERR_CUDA, "%s: cannot resolve the device status word", name);
   const double rope_base = rope.base == 0.0f ? 10000.0 : static_cast<double>(rope.base);
   return launched(rf::launch_attn_tc(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi,
                                      static_cast<rf::Dt>(dtype), st, sms > 0 ? ws : nullptr, sms, rope.mode,
@@ -359,7 +368,7 @@ rf_status_t rf_attn_decode_splitkv(const void* q, const void* k_cache, const voi
                            "rf_attn_decode_splitkv(split)");
   if (r != RF_OK) return r;
   return launched(rf::launch_lse_merge(o_part, lse_part, o, lse, int(rows), num_splits, D,
-                                       static_cast<rf::Dt>(dtype), s),
+                                       static_cast<rf::Dt>(dtype), st, s),
                   "rf_attn_decode_splitkv(merge)");
 }
 
@@ -377,8 +386,10 @@ rf_status_t rf_lse_merge(const float* o_part, const float* lse_part, void* o, fl
   RF_TRY(check_dev_ptr(lse_part, "lse_part"));
   RF_TRY(check_dev_ptr(o, "o"));
   RF_TRY(check_dev_ptr(lse, "lse"));
+  unsigned* st = rf::device_status_ptr();
+  if (!st) return fail(RF_ERR_CUDA, "rf_lse_merge: cannot resolve the device status word");
   return launched(rf::launch_lse_merge(o_part, lse_part, o, lse, rows, num_splits, D,
-                                       static_cast<rf::Dt>(out_dtype), static_cast<cudaStream_t>(stream)),
+                                       static_cast<rf::Dt>(out_dtype), st, static_cast<cudaStream_t>(stream)),
                   "rf_lse_merge");
 }
 
@@ -406,8 +417,10 @@ rf_status_t rf_layernorm_fused(const void* x, const void* residual, const void* 
   RF_TRY(check_dev_ptr(beta, "beta"));
   RF_TRY(check_dev_ptr(out, "out"));
   RF_TRY(check_dev_ptr(residual_out, "residual_out"));
+  unsigned* st = rf::device_status_ptr();
+  if (!st) return fail(RF_ERR_CUDA, "rf_layernorm_fused: cannot resolve the device status word");
   return launched(rf::launch_layernorm(x, residual, gamma, beta, out, residual_out, rows, cols, eps,
-                                       static_cast<rf::Dt>(dtype), static_cast<cudaStream_t>(stream)),
+                                       static_cast<rf::Dt>(dtype), st, static_cast<cudaStream_t>(stream)),
                   "rf_layernorm_fused");
 }
 
@@ -437,8 +450,10 @@ rf_status_t rf_rope_qk(const void* q, const void* k, void* q_out, void* k_out, i
   RF_TRY(check_dev_ptr(k, "k"));
   RF_TRY(check_dev_ptr(q_out, "q_out"));
   RF_TRY(check_dev_ptr(k_out, "k_out"));
+  unsigned* st = rf::device_status_ptr();
+  if (!st) return fail(RF_ERR_CUDA, "rf_rope_qk: cannot resolve the device status word");
   return launched(rf::launch_rope_qk(q, k, q_out, k_out, B * Hq, k ? B * Hkv : 0, N, D, static_cast<double>(base),
-                                     pos_offset, static_cast<rf::Dt>(dtype), static_cast<cudaStream_t>(stream)),
+                                     pos_offset, static_cast<rf::Dt>(dtype), st, static_cast<cudaStream_t>(stream)),
                   "rf_rope_qk");
 }
 
@@ -450,6 +465,12 @@ rf_status_t rf_selftest_wait_timeout(unsigned timeout_us, void* stream) {
   return launched(rf::launch_wait_timeout_selftest(uint64_t(timeout_us) * 1000u, st, nullptr,
                                                    static_cast<cudaStream_t>(stream)),
                   "rf_selftest_wait_timeout");
+}
+
+rf_status_t rf_selftest_check(void* stream) {
+  unsigned* st = rf::device_status_ptr();
+  if (!st) return fail(RF_ERR_CUDA, "rf_selftest_check: cannot resolve the device status word");
+  return launched(rf::launch_check_selftest(st, static_cast<cudaStream_t>(stream)), "rf_selftest_check");
 }
 
 rf_status_t rf_softmax_xent(const void* logits, const long long* targets, float* loss, float* lse, void* grad,
@@ -469,8 +490,10 @@ rf_status_t rf_softmax_xent(const void* logits, const long long* targets, float*
   RF_TRY(check_dev_ptr(loss, "loss"));
   RF_TRY(check_dev_ptr(lse, "lse"));
   RF_TRY(check_dev_ptr(grad, "grad"));
+  unsigned* st = rf::device_status_ptr();
+  if (!st) return fail(RF_ERR_CUDA, "rf_softmax_xent: cannot resolve the device status word");
   return launched(rf::launch_xent(logits, targets, loss, lse, grad, rows, vocab, ignore_index,
-                                  static_cast<rf::Dt>(dtype), static_cast<cudaStream_t>(stream)),
+                                  static_cast<rf::Dt>(dtype), st, static_cast<cudaStream_t>(stream)),
                   "rf_softmax_xent");
 }
 
@@ -495,8 +518,10 @@ rf_status_t rf_rmsnorm_fused(const void* x, const void* residual, const void* ga
   RF_TRY(check_dev_ptr(gamma, "gamma"));
   RF_TRY(check_dev_ptr(out, "out"));
   RF_TRY(check_dev_ptr(residual_out, "residual_out"));
+  unsigned* st = rf::device_status_ptr();
+  if (!st) return fail(RF_ERR_CUDA, "rf_rmsnorm_fused: cannot resolve the device status word");
   return launched(rf::launch_rmsnorm(x, residual, gamma, out, residual_out, rows, cols, eps,
-                                     static_cast<rf::Dt>(dtype), static_cast<cudaStream_t>(stream)),
+                                     static_cast<rf::Dt>(dtype), st, static_cast<cudaStream_t>(stream)),
                   "rf_rmsnorm_fused");
 }
 

@@ -20,6 +20,24 @@ namespace rf {
 
 // Status codes a kernel ORs into the device status word.
 constexpr unsigned kStatusTimeout = 1u;
+constexpr unsigned kStatusCheck = 2u;  // an index check of an RF_CHECKS build failed
+
+// Index checks (built with -DRF_CHECKS): RF_INB(cond, status) is true when the
+// computed index `cond` describes lies inside its buffer; otherwise it records
+// kStatusCheck in the device status word and is false, and the caller skips
+// the access it guards.  Nothing traps.  Other builds compile it to `true`
+// without evaluating `cond`.
+#ifdef RF_CHECKS
+__device__ __forceinline__ bool in_bounds_checked(bool ok, unsigned* status) {
+  if (!ok) atomicOr(status, kStatusCheck);
+  return ok;
+}
+#define RF_INB(cond, status) (::rf::in_bounds_checked((cond), (status)))
+constexpr bool kChecks = true;
+#else
+#define RF_INB(cond, status) true
+constexpr bool kChecks = false;
+#endif
 
 // ---------------------------------------------------------------- conversions
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }

@@ -15,24 +15,24 @@ enum class Dt : int { F32 = 0, F16 = 1, BF16 = 2 };
 int layernorm_max_cols(Dt dt);
 cudaError_t launch_layernorm(const void* x, const void* r, const void* gamma, const void* beta,
                              void* out, void* r_out, int rows, int cols, float eps, Dt dt,
-                             cudaStream_t s);
+                             unsigned* status, cudaStream_t s);
 
 // residual + RMSNorm (ln_fused.cu; same limits as LayerNorm)
 cudaError_t launch_rmsnorm(const void* x, const void* r, const void* gamma, void* out, void* r_out, int rows,
-                           int cols, float eps, Dt dt, cudaStream_t s);
+                           int cols, float eps, Dt dt, unsigned* status, cudaStream_t s);
 
 // softmax cross-entropy per row, optional gradient (xent_fused.cu)
 cudaError_t launch_xent(const void* logits, const long long* targets, float* loss, float* lse, void* grad, int rows,
-                        int vocab, long long ignore_index, Dt dt, cudaStream_t s);
+                        int vocab, long long ignore_index, Dt dt, unsigned* status, cudaStream_t s);
 
 // log-sum-exp merge of split partials (lse_merge.cu)
 cudaError_t launch_lse_merge(const float* o_part, const float* lse_part, void* o, float* lse,
-                             int rows, int splits, int D, Dt out_dt, cudaStream_t s);
+                             int rows, int splits, int D, Dt out_dt, unsigned* status, cudaStream_t s);
 
 // exact fp32 SIMT attention forward (attn_fwd_f32.cu)
 cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, float* o, float* lse,
                             int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal,
-                            int window, const float* alibi, cudaStream_t s);
+                            int window, const float* alibi, unsigned* status, cudaStream_t s);
 
 // split-KV decode partials (decode_split.cu): writes o_part [B*Hq, S, D] and
 // lse_part [B*Hq, S] fp32.
@@ -71,6 +71,8 @@ int device_sm_count();
 
 // bounded-wait failure path self-test (selftest.cu)
 cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, unsigned* status, int* waited_out, cudaStream_t s);
+// an index check that always fails, with no memory access (selftest.cu)
+cudaError_t launch_check_selftest(unsigned* status, cudaStream_t s);
 
 // fusion-level / incremental-form ablation variants (ablation.cu)
 constexpr int kLnSmemMaxCols = 56832;  // variant 1 stages cols floats in shared memory
@@ -85,7 +87,7 @@ cudaError_t launch_xent_ablation(const void* logits, const long long* targets, f
 // D in {64, 128, 256}; q_out / k_out may alias q / k
 constexpr int kRopeMaxHalf = 128;
 cudaError_t launch_rope_qk(const void* q, const void* k, void* q_out, void* k_out, int BHq, int BHkv, int N, int D,
-                           double base, int pos_offset, Dt dt, cudaStream_t s);
+                           double base, int pos_offset, Dt dt, unsigned* status, cudaStream_t s);
 
 // TMA descriptor encoding through the driver entry point (rf_api.cu).
 // 3-D tensor [outer][rows][inner] of 16-bit elements, box {64, box_rows, 1},

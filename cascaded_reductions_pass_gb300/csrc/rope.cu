@@ -59,7 +59,7 @@ __device__ __forceinline__ uint4 rotate(const uint4& a, const uint4& b, const fl
 template <Dt DT, int D, int NBC>
 __device__ __forceinline__ void rotate_rows(const uint4* __restrict__ q, const uint4* __restrict__ k,
                                             uint4* __restrict__ qo, uint4* __restrict__ ko, int BHq, int BHkv,
-                                            int N, int n0, int nb_rt, const float2* cs) {
+                                            int N, int n0, int nb_rt, const float2* cs, unsigned* status) {
   constexpr int CP = D / 16;  // chunk pairs per row
   constexpr int RS = CsLayout<D>::RS;
   constexpr int RV = D / 8;   // 16-byte chunks per row
@@ -82,6 +82,7 @@ __device__ __forceinline__ void rotate_rows(const uint4* __restrict__ q, const u
       const int bh = r / nb;
       nl[u] = r - bh * nb;
       row[u] = (static_cast<long long>(bh) * N + n0 + nl[u]) * RV;
+      if (live[u]) live[u] = RF_INB(bh < (isq[u] ? BHq : BHkv) && n0 + nl[u] < N && nl[u] < nb, status);
       if (live[u]) {
         const uint4* src = isq[u] ? q : k;
         a[u] = ld_stream(src + row[u] + cp[u]);
@@ -104,7 +105,7 @@ template <Dt DT, int D>
 __global__ void __launch_bounds__(kThreads) rope_kernel(const uint4* __restrict__ q, const uint4* __restrict__ k,
                                                         uint4* __restrict__ qo, uint4* __restrict__ ko, int BHq,
                                                         int BHkv, int N, int pos_offset,
-                                                        const __grid_constant__ RopeParams prm) {
+                                                        const __grid_constant__ RopeParams prm, unsigned* status) {
   constexpr int H2 = D / 2;
   constexpr int CP = CsLayout<D>::CP, RS = CsLayout<D>::RS;
   __shared__ float2 cs[kNB * RS];
@@ -117,24 +118,24 @@ __global__ void __launch_bounds__(kThreads) rope_kernel(const uint4* __restrict_
   __syncthreads();
 
   if (nb == kNB) {
-    rotate_rows<DT, D, kNB>(q, k, qo, ko, BHq, BHkv, N, n0, kNB, cs);
+    rotate_rows<DT, D, kNB>(q, k, qo, ko, BHq, BHkv, N, n0, kNB, cs, status);
   } else {
-    rotate_rows<DT, D, 0>(q, k, qo, ko, BHq, BHkv, N, n0, nb, cs);
+    rotate_rows<DT, D, 0>(q, k, qo, ko, BHq, BHkv, N, n0, nb, cs, status);
   }
 }
 
 template <Dt DT>
 cudaError_t launch_dt(const void* q, const void* k, void* qo, void* ko, int BHq, int BHkv, int N, int D,
-                      int pos_offset, const RopeParams& prm, cudaStream_t s) {
+                      int pos_offset, const RopeParams& prm, unsigned* status, cudaStream_t s) {
   const unsigned grid = static_cast<unsigned>((N + kNB - 1) / kNB);
   auto Q = static_cast<const uint4*>(q);
   auto K = static_cast<const uint4*>(k);
   auto QO = static_cast<uint4*>(qo);
   auto KO = static_cast<uint4*>(ko);
   switch (D) {
-    case 64: rope_kernel<DT, 64><<<grid, kThreads, 0, s>>>(Q, K, QO, KO, BHq, BHkv, N, pos_offset, prm); break;
-    case 128: rope_kernel<DT, 128><<<grid, kThreads, 0, s>>>(Q, K, QO, KO, BHq, BHkv, N, pos_offset, prm); break;
-    case 256: rope_kernel<DT, 256><<<grid, kThreads, 0, s>>>(Q, K, QO, KO, BHq, BHkv, N, pos_offset, prm); break;
+    case 64: rope_kernel<DT, 64><<<grid, kThreads, 0, s>>>(Q, K, QO, KO, BHq, BHkv, N, pos_offset, prm, status); break;
+    case 128: rope_kernel<DT, 128><<<grid, kThreads, 0, s>>>(Q, K, QO, KO, BHq, BHkv, N, pos_offset, prm, status); break;
+    case 256: rope_kernel<DT, 256><<<grid, kThreads, 0, s>>>(Q, K, QO, KO, BHq, BHkv, N, pos_offset, prm, status); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -143,11 +144,11 @@ cudaError_t launch_dt(const void* q, const void* k, void* qo, void* ko, int BHq,
 }  // namespace
 
 cudaError_t launch_rope_qk(const void* q, const void* k, void* q_out, void* k_out, int BHq, int BHkv, int N, int D,
-                           double base, int pos_offset, Dt dt, cudaStream_t s) {
+                           double base, int pos_offset, Dt dt, unsigned* status, cudaStream_t s) {
   const RopeParams prm = make_rope_params(base, D);
   switch (dt) {
-    case Dt::F16: return launch_dt<Dt::F16>(q, k, q_out, k_out, BHq, BHkv, N, D, pos_offset, prm, s);
-    case Dt::BF16: return launch_dt<Dt::BF16>(q, k, q_out, k_out, BHq, BHkv, N, D, pos_offset, prm, s);
+    case Dt::F16: return launch_dt<Dt::F16>(q, k, q_out, k_out, BHq, BHkv, N, D, pos_offset, prm, status, s);
+    case Dt::BF16: return launch_dt<Dt::BF16>(q, k, q_out, k_out, BHq, BHkv, N, D, pos_offset, prm, status, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -1,8 +1,10 @@
-// selftest.cu -- exercises the bounded-wait failure path on the GPU without
-// hanging or faulting it: one warp waits on an mbarrier that nothing arrives
+// selftest.cu -- exercises the failure paths on the GPU without hanging or
+// faulting it.  The bounded-wait path: one warp waits on an mbarrier that nothing arrives
 // on, gives up after a short limit, records RF_ERR_TIMEOUT in the device
 // status word exactly as the production kernels do, and returns.  Nothing is
 // in flight (no TMA copy, no tensor-memory allocation) when it gives up.
+// The index-check path of RF_CHECKS builds: one thread evaluates a check that
+// fails, with no memory access behind it.
 #include "rf_device.cuh"
 
 namespace rf {
@@ -22,7 +24,18 @@ __global__ void __launch_bounds__(32) wait_timeout_kernel(uint64_t limit_ns, uns
   }
 }
 
+// An index that lies past a (phantom) buffer of 8 elements: the check fails
+// and, in a checked build, records kStatusCheck; no access is made either way.
+__global__ void __launch_bounds__(32) check_kernel(unsigned* status, int idx) {
+  if (threadIdx.x == 0) (void)RF_INB(idx < 8, status);
+}
+
 }  // namespace
+
+cudaError_t launch_check_selftest(unsigned* status, cudaStream_t s) {
+  check_kernel<<<1, 32, 0, s>>>(status, 8);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, unsigned* status, int* waited_out, cudaStream_t s) {
   wait_timeout_kernel<<<1, 32, 0, s>>>(limit_ns, status, waited_out);

@@ -164,10 +164,12 @@ template <Dt DT, int NT>
 __global__ void __launch_bounds__(NT) xent_kernel(const uint4* __restrict__ logits,
                                                   const long long* __restrict__ targets,
                                                   float* __restrict__ loss, float* __restrict__ lse_out,
-                                                  uint4* __restrict__ grad, int nvec, long long ignore_index) {
+                                                  uint4* __restrict__ grad, int nvec, long long ignore_index,
+                                                  int rows, unsigned* status) {
   constexpr int E = Pack<DT>::E;
   __shared__ Run s_run[NT / 32];
   const long long row = blockIdx.x;
+  if (!RF_INB(row < rows, status)) return;
   const uint4* zr = logits + row * nvec;
   const Run run = cta_combine<NT>(fold_range<DT, NT>(zr, 0, nvec), s_run);
   const float lse2 = run.m + log2f(run.l);  // base 2
@@ -188,7 +190,8 @@ __global__ void __launch_bounds__(kThreads) xent_cluster_kernel(const uint4* __r
                                                                 float* __restrict__ loss,
                                                                 float* __restrict__ lse_out,
                                                                 uint4* __restrict__ grad, int nvec,
-                                                                long long ignore_index) {
+                                                                long long ignore_index, int rows,
+                                                                unsigned* status) {
   constexpr int E = Pack<DT>::E;
   __shared__ Run s_run[kThreads / 32];
   __shared__ Run s_part;   // this CTA's (m, l), read by rank 0
@@ -199,11 +202,14 @@ __global__ void __launch_bounds__(kThreads) xent_cluster_kernel(const uint4* __r
   const long long row = blockIdx.x / cs;
   const int c0 = static_cast<int>(static_cast<long long>(nvec) * rank / cs);
   const int c1 = static_cast<int>(static_cast<long long>(nvec) * (rank + 1) / cs);
-  const uint4* zr = logits + row * nvec;
-  const Run part = cta_combine<kThreads>(fold_range<DT, kThreads>(zr, c0, c1), s_run);
+  // every CTA of the cluster meets the cluster barriers below, so a failed
+  // check only empties its slice
+  const bool in_row = RF_INB(row < rows && c0 >= 0 && c0 <= c1 && c1 <= nvec, status);
+  const uint4* zr = logits + (in_row ? row : 0) * nvec;
+  const Run part = cta_combine<kThreads>(fold_range<DT, kThreads>(zr, in_row ? c0 : 0, in_row ? c1 : 0), s_run);
   if (threadIdx.x == 0) s_part = part;
   cluster.sync();  // every slice's (m, l) is in its CTA's shared memory
-  if (rank == 0 && threadIdx.x == 0) {
+  if (rank == 0 && threadIdx.x == 0 && in_row) {
     Run run = s_part;
     for (int r = 1; r < cs; ++r) run = lse_combine(run, *cluster.map_shared_rank(&s_part, r));
     const float lse2 = run.m + log2f(run.l);
@@ -214,7 +220,7 @@ __global__ void __launch_bounds__(kThreads) xent_cluster_kernel(const uint4* __r
     loss[row] = row_loss<DT>(logits, row, static_cast<long long>(nvec) * E, t, ignore_index, lse);
   }
   cluster.sync();  // s_lse2 is set everywhere; no CTA reads another's shared memory after this
-  if (grad) {
+  if (grad && in_row) {
     const long long t = targets[row];
     write_grad<DT, kThreads>(zr, grad + row * nvec, c0, c1, s_lse2, t, t == ignore_index);
   }
@@ -231,14 +237,15 @@ int xent_cluster_size(int rows, int nvec, int sms) {
 
 template <Dt DT>
 cudaError_t launch_dt(const uint4* L, const long long* targets, float* loss, float* lse, uint4* G, int rows,
-                      int nvec, long long ignore_index, int sms, cudaStream_t s) {
+                      int nvec, long long ignore_index, int sms, unsigned* status, cudaStream_t s) {
   const int cs = xent_cluster_size(rows, nvec, sms);
   if (cs == 1) {
     // rows of fewer than kShortRowVecs vectors: CTAs of half the size (more rows in flight per SM)
     if (nvec < kShortRowVecs)
-      xent_kernel<DT, kThreads / 2><<<rows, kThreads / 2, 0, s>>>(L, targets, loss, lse, G, nvec, ignore_index);
+      xent_kernel<DT, kThreads / 2><<<rows, kThreads / 2, 0, s>>>(L, targets, loss, lse, G, nvec, ignore_index, rows,
+                                                                   status);
     else
-      xent_kernel<DT, kThreads><<<rows, kThreads, 0, s>>>(L, targets, loss, lse, G, nvec, ignore_index);
+      xent_kernel<DT, kThreads><<<rows, kThreads, 0, s>>>(L, targets, loss, lse, G, nvec, ignore_index, rows, status);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -253,22 +260,22 @@ cudaError_t launch_dt(const uint4* L, const long long* targets, float* loss, flo
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, xent_cluster_kernel<DT>, L, targets, loss, lse, G, nvec, ignore_index);
+  return cudaLaunchKernelEx(&cfg, xent_cluster_kernel<DT>, L, targets, loss, lse, G, nvec, ignore_index, rows, status);
 }
 
 }  // namespace
 
 cudaError_t launch_xent(const void* logits, const long long* targets, float* loss, float* lse, void* grad, int rows,
-                        int vocab, long long ignore_index, Dt dt, cudaStream_t s) {
+                        int vocab, long long ignore_index, Dt dt, unsigned* status, cudaStream_t s) {
   const int E = dt == Dt::F32 ? 4 : 8;
   const int nvec = vocab / E;
   const int sms = device_sm_count();
   auto L = static_cast<const uint4*>(logits);
   auto G = static_cast<uint4*>(grad);
   switch (dt) {
-    case Dt::F32: return launch_dt<Dt::F32>(L, targets, loss, lse, G, rows, nvec, ignore_index, sms, s);
-    case Dt::F16: return launch_dt<Dt::F16>(L, targets, loss, lse, G, rows, nvec, ignore_index, sms, s);
-    case Dt::BF16: return launch_dt<Dt::BF16>(L, targets, loss, lse, G, rows, nvec, ignore_index, sms, s);
+    case Dt::F32: return launch_dt<Dt::F32>(L, targets, loss, lse, G, rows, nvec, ignore_index, sms, status, s);
+    case Dt::F16: return launch_dt<Dt::F16>(L, targets, loss, lse, G, rows, nvec, ignore_index, sms, status, s);
+    case Dt::BF16: return launch_dt<Dt::BF16>(L, targets, loss, lse, G, rows, nvec, ignore_index, sms, status, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -48,7 +48,8 @@ typedef enum {
   RF_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misalignment, short workspace */
   RF_ERR_UNSUPPORTED = 2,  /* well-formed but not implemented (e.g. head dim) */
   RF_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
-  RF_ERR_TIMEOUT = 4       /* a bounded device-side wait ran out (rf_device_status) */
+  RF_ERR_TIMEOUT = 4,      /* a bounded device-side wait ran out (rf_device_status) */
+  RF_ERR_CHECK = 5         /* an index check of a checked build failed (rf_device_status) */
 } rf_status_t;
 
 typedef enum { RF_F32 = 0, RF_F16 = 1, RF_BF16 = 2 } rf_dtype_t;
@@ -353,8 +354,27 @@ const char* rf_last_error(void);
 int rf_version(void);
 
 /*
+ * rf_checks_enabled -- 1 when the library was built with -DRF_CHECKS, else 0.
+ * In such a build every kernel checks the indices it computes (tensor
+ * coordinates, output rows and offsets, split-tail and workspace slots, shared
+ * memory tiles) before it uses them; a check that fails skips the access,
+ * never traps, and records RF_ERR_CHECK for rf_device_status.  It stands in
+ * for a memory checker on machines where none may run.
+ */
+int rf_checks_enabled(void);
+
+/*
+ * rf_selftest_check -- launches one thread that evaluates an index check
+ * which always fails, without touching memory: in a checked build the device
+ * status word then reports RF_ERR_CHECK (rf_device_status); in other builds
+ * nothing is recorded.  RF_ERR_CUDA if the launch fails.
+ */
+rf_status_t rf_selftest_check(void* stream);
+
+/*
  * rf_device_status -- synchronise `stream`, then report whether any kernel of
- * this library on the current device recorded a bounded wait that ran out
+ * this library on the current device recorded a failed index check
+ * (RF_ERR_CHECK, checked builds only) or else a bounded wait that ran out
  * (RF_ERR_TIMEOUT) since the status was last cleared; clear != 0 resets it.
  * Returns RF_ERR_CUDA if the synchronisation itself fails.
  */

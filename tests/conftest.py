@@ -29,15 +29,16 @@ def rf():
 @pytest.fixture(autouse=True)
 def _no_silent_timeout(request):
     """After every GPU test: no kernel may have recorded a bounded wait that ran
-    out (RF_ERR_TIMEOUT in the device status word) without the test clearing
-    it.  Results can still look right when a wait gives up in a CTA whose work
+    out (RF_ERR_TIMEOUT in the device status word), or in a checked build a
+    failed index check (RF_ERR_CHECK), without the test clearing it.  Results can still look right when a wait gives up in a CTA whose work
     was already done, so parity alone would not catch it."""
     yield
     if request.node.get_closest_marker("gpu") is None or "rf" not in request.fixturenames:
         return
     rfmod = request.getfixturevalue("rf")
     status = rfmod.rf_device_status(clear=True)
-    assert status == rfmod.RF_OK, f"a kernel recorded a bounded-wait timeout during {request.node.nodeid}"
+    assert status == rfmod.RF_OK, (f"a kernel recorded {rfmod.STATUS_NAMES.get(status, status)} "
+                                   f"(a bounded wait that ran out, or a failed index check) during {request.node.nodeid}")
 
 
 # A planted-mistake run of the oracle pin suite (see _oracle_mutants.py): the

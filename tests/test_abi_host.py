@@ -32,6 +32,10 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, name)
 
 
+def test_regular_build_has_no_index_checks(lib):
+    assert lib.rf_checks_enabled() == 0
+
+
 def test_version(lib):
     assert lib.rf_version() == 10100  # 1.1.0: rotary embedding fields in rf_attn_opts_t
 
