@@ -167,7 +167,7 @@ class Runner:
             self.bytes = workmodel.attn_bytes(d["B"], d["Hq"], d["Hkv"], d["N"], d["N"], d["D"], self.dtype)
             self.metric, self.unit, self.bound = METRICS["attn"]
             self.units = self.flops / 1e12
-            self.kernel_file = "attn_fwd_f32.cu" if self.dtype == "f32" else "attn_fwd_tc.cu"
+            self.kernel_file = "attn_fwd_f32.cu" if self.dtype == "f32" else "attn_fwd_tc.cuh"
             self.kernel = "attn_fwd_f32" if self.dtype == "f32" else "attn_fwd_tc"
             if self.dtype != "f32" and d["D"] == 64 and 0 < self.window <= 1024:  # the persistent windowed kernel
                 self.kernel_file, self.kernel = "attn_fwd_tc_window.cu", "attn_fwd_tc_window"
