@@ -126,6 +126,26 @@ int device_sm_count() {
   return counts[dev];
 }
 
+long long device_l2_bytes() {
+  static std::mutex mu;
+  static long long bytes[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 0;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if (bytes[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    bytes[dev] = n;
+  }
+  return bytes[dev];
+}
+
 bool encode_tma_3d_16bit(void* tmap_out, const void* base, uint64_t inner, uint64_t rows,
                          uint64_t outer, uint32_t box_rows, cudaError_t* err) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;

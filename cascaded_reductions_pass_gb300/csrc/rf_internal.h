@@ -68,6 +68,8 @@ cudaError_t launch_attn_tc_window(const void* q, const void* k, const void* v, v
 
 // multiprocessor count of the current device (cached per device; 0 on error)
 int device_sm_count();
+// L2 cache size in bytes of the current device (cached per device; 0 on error)
+long long device_l2_bytes();
 
 // bounded-wait failure path self-test (selftest.cu)
 cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, unsigned* status, int* waited_out, cudaStream_t s);

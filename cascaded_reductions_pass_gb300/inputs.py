@@ -126,6 +126,9 @@ WORKLOADS = {
                                    dict(B=4, Hq=12, Hkv=12, N=4096, D=64, causal=1, window=256)),
     "attn_causal_alibi_f16_d64": Workload("attn_causal_alibi_f16_d64", "attn", "f16", 9,
                                           dict(B=4, Hq=12, Hkv=12, N=4096, D=64, causal=1, alibi=1)),
+    # the exact fp32 path at a size where its FFMA throughput, not launch latency, decides
+    "attn_f32_d64_n2048": Workload("attn_f32_d64_n2048", "attn", "f32", 11,
+                                   dict(B=1, Hq=8, Hkv=8, N=2048, D=64, causal=0)),
     # rotary embedding of Q and K at AttnFuse's RoPE + causal shape (Tables 4-5)
     "rope_qk_f16_d64": Workload("rope_qk_f16_d64", "rope", "f16", 10,
                                 dict(B=4, Hq=12, Hkv=12, N=4096, D=64, base=10000.0)),
