@@ -189,7 +189,9 @@ size_t rf_attn_decode_splitkv_workspace_bytes(int B, int Hq, int D, int num_spli
  * 1 <= num_splits <= 256.  Pointers 16-byte aligned.
  * Errors: RF_ERR_INVALID_ARG for null pointers, non-positive sizes,
  * Hq % Hkv != 0, misalignment, or a short workspace; RF_ERR_UNSUPPORTED for
- * other dtype / D / group size; RF_ERR_CUDA if a launch fails.
+ * other dtype / D / group size; RF_ERR_CUDA if a launch fails.  A split whose
+ * bounded wait runs out (reported later by rf_device_status as
+ * RF_ERR_TIMEOUT) writes NaN partials, so the rows it feeds come out NaN.
  */
 rf_status_t rf_attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
                                    void* o, float* lse, void* workspace, size_t workspace_bytes,
@@ -218,8 +220,9 @@ rf_status_t rf_attn_decode_splitkv(const void* q, const void* k_cache, const voi
  *   capture.
  * - All calls share the one scratch array: calls that can overlap on the GPU
  *   (other streams, other host threads) race on it and must be serialised by
- *   the caller.  After a call the array holds that call's partials; nothing
- *   in it needs to start at zero.
+ *   the caller.  After a call the array holds that call's partials (NaN for
+ *   a split whose bounded wait ran out, which also makes its rows' outputs
+ *   NaN); nothing in it needs to start at zero.
  */
 #define RF_DECODE_NOALLOC_SCRATCH_BYTES (16u << 20) /* 16 MiB */
 rf_status_t rf_attn_decode_splitkv_noalloc(const void* q, const void* k_cache, const void* v_cache,
@@ -237,7 +240,10 @@ rf_status_t rf_attn_decode_splitkv_noalloc(const void* q, const void* k_cache, c
  *   lse_part [rows, num_splits]    fp32 (read; -inf marks an empty part)
  *   o        [rows, D]             out_dtype (written)
  *   lse      [rows]                fp32, nullable (written)
- *   A row whose parts are all empty gets O = 0 and LSE = -inf.
+ *   A row whose parts are all empty gets O = 0 and LSE = -inf.  A part whose
+ *   lse_s is NaN (a split that gave up after a bounded wait writes that) makes
+ *   the row's O and LSE NaN.  Each weight is formed as exp(lse_s - max) / sum
+ *   over the row's parts, so the rounding of LSE does not enter the weights.
  *
  * Supported: out_dtype RF_F32 / RF_F16 / RF_BF16, D a multiple of 4 up to 512,
  * 1 <= num_splits <= 256.  o_part and o 16-byte aligned.
@@ -250,10 +256,13 @@ rf_status_t rf_lse_merge(const float* o_part, const float* lse_part, void* o, fl
 
 /*
  * rf_layernorm_fused -- residual add + LayerNorm in one pass over each row:
- * h = x + residual; mean and biased variance of h (running count / mean / M2
- * updated per element and merged across threads with the pairwise combine);
- * y = (h - mean) / sqrt(var + eps) * gamma + beta ("Operator Fusion" guide,
- * section 1 and section 2 Pattern 2; section 4 places eps inside the root).
+ * h = x + residual; mean and biased variance of h from running sums of
+ * (h - K) and (h - K)^2 about K, the mean of the row's first 16-byte vector,
+ * merged across threads by addition (a row whose K lies more than one standard
+ * deviation from its mean recomputes the variance about the mean from the
+ * values it holds); y = ((h - K) - (mean - K)) / sqrt(var + eps) * gamma + beta
+ * ("Operator Fusion" guide, section 1 and section 2 Pattern 2; section 4
+ * places eps inside the root).
  * The row is kept on chip between the statistics and the normalisation, so
  * x and residual are read once and y written once.
  *
@@ -358,8 +367,8 @@ int rf_version(void);
  * In such a build every kernel checks the indices it computes (tensor
  * coordinates, output rows and offsets, split-tail and workspace slots, shared
  * memory tiles) before it uses them; a check that fails skips the access,
- * never traps, and records RF_ERR_CHECK for rf_device_status.  It stands in
- * for a memory checker on machines where none may run.
+ * never traps, and records RF_ERR_CHECK for rf_device_status.  The checks run
+ * inside the kernels, at full size, with no external tool.
  */
 int rf_checks_enabled(void);
 
