@@ -8,17 +8,28 @@
 // exp(m_old - m_new) and the tile's terms are added.  O = acc / l and
 // LSE = m + ln l at the end.  fp32 tensor-core modes (TF32) round the
 // operands to 10 mantissa bits, too coarse for a 1e-5 relative result, so
-// this path uses FFMA throughout with the accurate expf/logf.
+// this path uses FFMA throughout with the accurate exp2f/log2f.
 //
-// CTA: 4 warps, 16 query rows (4 per warp), key tiles of 32 (one key per
-// lane) staged in shared memory with K rows padded to D+4 floats.  Each warp
-// forms the scores of its four rows together, so a lane reads its key's K row
-// once per tile for all four; the exponentials are base 2 (log2 e folded into
-// the scale) through exp2f, accurate to 2 ulp; the probabilities go through
-// shared memory, where the output update reads four keys of a row with one
-// broadcast load.  With the causal mask a sliding window (key j visible to
-// query i iff i - window < j) and ALiBi biases (+ slope_h * (j - i)) are
-// supported as in the tensor-core path.
+// CTA: 64 query rows, 8 warps in two groups of 4.  The CTA's key tiles are
+// split in two contiguous halves, one per group (the split of RedFuser's
+// Figure 13, inside the CTA): warp w takes rows 16 (w mod 4) .. + 15 over
+// the keys of group w / 4, and the two groups' (m, l, acc) states are merged
+// once at the end.  Both products are register-tiled micro-GEMMs: lane =
+// 8 rg + g (row group rg < 4, column group g < 8) holds rows rg + 4i (i < 4)
+// of its warp, and
+//   S = Q K^T   the keys g + 8i' (i' < 4) of the tile: 16 scores per lane,
+//               64 FFMA per four Q and four K float4 loads;
+//   O += P V    the output columns 4g + 32c + e (c < NC, e < 4): 16 NC
+//               accumulators, 16 NC FFMA per key from one P and NC V float4.
+// Row max and row sum finish with three shuffles inside the 8-lane group.
+// Each group double-buffers its K and V tiles in shared memory by cp.async
+// (the next tile streams in while the current one is used) and synchronises
+// on a named barrier of its own; K and Q rows are padded to
+// a stride of 4 (mod 32) words and P rows to 40 words, so every shared-memory
+// access of a warp is conflict-free.  Exponentials are base 2 (log2 e folded
+// into the scale) through exp2f, accurate to 2 ulp.  With the causal mask a
+// sliding window (key j visible to query i iff i - window < j) and ALiBi
+// biases (+ slope_h * (j - i)) are supported as in the tensor-core path.
 #include <math.h>
 
 #include "rf_device.cuh"
@@ -26,31 +37,68 @@
 namespace rf {
 namespace {
 
-constexpr int kRowsPerWarp = 4;
-constexpr int kWarps = 4;
-constexpr int kBM = kRowsPerWarp * kWarps;  // 16 query rows per CTA
-constexpr int kBN = 32;                     // keys per tile
+constexpr int kGroupWarps = 4;           // warps per key group
+constexpr int kGroups = 2;               // key groups per CTA
+constexpr int kWarps = kGroupWarps * kGroups;
+constexpr int kRowsW = 16;               // query rows per warp
+constexpr int kBM = kGroupWarps * kRowsW;  // 64 query rows per CTA
+constexpr int kBN = 32;                  // keys per tile
+constexpr int kPS = 40;                  // P row stride (words)
 
-template <int DC>  // DC = ceil(D / 32) output columns per lane
+__host__ __device__ __forceinline__ int padded_stride(int D) { return (D + 31) / 32 * 32 + 4; }
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void group_barrier(int id) {  // the 128 threads of one key group
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(kGroupWarps * 32) : "memory");
+}
+
+__device__ __forceinline__ float group_max(float v) {  // over the 8 lanes of a row group
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+  return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+}
+__device__ __forceinline__ float group_sum(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+  v += __shfl_xor_sync(0xffffffffu, v, 2);
+  return v + __shfl_xor_sync(0xffffffffu, v, 4);
+}
+
+// NC = ceil(D / 32): float4 output groups per lane.  DC: the head dimension
+// fixed at compile time (so that every shared-memory offset is an immediate
+// and the loops over D unroll), or 0 for any D <= 32 NC.
+template <int NC, int DC>
 __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const float* __restrict__ q,
                                                                const float* __restrict__ k,
                                                                const float* __restrict__ v, float* __restrict__ o,
                                                                float* __restrict__ lse, int Hq, int Hkv, int Nq,
-                                                               int Nk, int D, float scale, int causal, int window,
+                                                               int Nk, int Dn, float scale, int causal, int window,
                                                                const float* __restrict__ alibi, unsigned* status) {
+  static_assert(DC == 0 || (DC % 4 == 0 && DC <= 32 * NC && DC > 32 * (NC - 1)), "DC must match NC");
   extern __shared__ float4 smem4[];
   float* smem = reinterpret_cast<float*>(smem4);
-  const int KS = D + 4;               // padded K row stride (floats)
-  float* Qs = smem;                   // [kBM][D]
-  float* Ks = Qs + kBM * D;           // [kBN][KS]
-  float* Vs = Ks + kBN * KS;          // [kBN][D]
-  float* Ps = Vs + kBN * D;           // [kWarps][kRowsPerWarp][kBN] probabilities of the tile
-
+  const int D = DC ? DC : Dn;
+  const int KS = padded_stride(D);  // Q and K row stride (words)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = warp / kGroupWarps, wr = warp % kGroupWarps;  // key group; row block of the warp
+  const int gtid = threadIdx.x % (kGroupWarps * 32);            // thread index within the group
+  const int rg = lane >> 3, g = lane & 7;
+  float* Qs = smem;                                 // [kBM][KS]
+  float* Ks = Qs + kBM * KS + grp * (2 * kBN * KS);  // this group's [2][kBN][KS]
+  float* Vs = Qs + kBM * KS + kGroups * 2 * kBN * KS + grp * (2 * kBN * D);  // this group's [2][kBN][D]
+  float* Ps = Qs + kBM * KS + kGroups * 2 * kBN * (KS + D);  // [kWarps][kRowsW][kPS]
   const int b = blockIdx.z, h = blockIdx.y, hk = h / (Hq / Hkv);
   const int q0 = blockIdx.x * kBM;
   // the grid is (query blocks, Hq, B): a block past them has nothing to do
-  if (!RF_INB(q0 < Nq && h < Hq && hk < Hkv && D <= 32 * DC, status)) return;
+  if (!RF_INB(q0 < Nq && h < Hq && hk < Hkv && D <= 32 * NC && (D & 3) == 0 && Dn == D, status)) return;
   const float* qh = q + (static_cast<long long>(b) * Hq + h) * Nq * D;
   const float* kh = k + (static_cast<long long>(b) * Hkv + hk) * Nk * D;
   const float* vh = v + (static_cast<long long>(b) * Hkv + hk) * Nk * D;
@@ -58,114 +106,208 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const float* __re
   constexpr float kLog2e = 1.4426950408889634f;
   const float sl2 = scale * kLog2e;  // scores in base-2 units
 
-  for (int i = threadIdx.x; i < kBM * D4; i += blockDim.x) {
-    const int r = i / D4, c = i - r * D4;
-    float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (q0 + r < Nq) val = reinterpret_cast<const float4*>(qh + static_cast<long long>(q0 + r) * D)[c];
-    reinterpret_cast<float4*>(Qs + r * D)[c] = val;
-  }
-
-  float m[kRowsPerWarp], l[kRowsPerWarp], acc[kRowsPerWarp][DC];
-#pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) {
-    m[r] = -INFINITY;
-    l[r] = 0.f;
-#pragma unroll
-    for (int c = 0; c < DC; ++c) acc[r][c] = 0.f;
-  }
-
   const int last_row = min(q0 + kBM, Nq) - 1;
   const int kend = causal ? min(Nk, last_row + 1) : Nk;  // keys past the CTA's last row are all masked
   // a sliding window hides every key below the first row's window
   const int kbeg = (causal && window > 0) ? (max(0, q0 - window + 1) / kBN) * kBN : 0;
-  const float slope2 = alibi ? __ldg(alibi + h) * kLog2e : 0.f;
-  const float* qw_rows = Qs + warp * kRowsPerWarp * D;
-  float* pw = Ps + warp * kRowsPerWarp * kBN;
-  for (int k0 = kbeg; k0 < kend; k0 += kBN) {
-    __syncthreads();
-    for (int i = threadIdx.x; i < kBN * D4; i += blockDim.x) {
-      const int r = i / D4, c = i - r * D4;
-      float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
-      if (k0 + r < Nk) {
-        kv = reinterpret_cast<const float4*>(kh + static_cast<long long>(k0 + r) * D)[c];
-        vv = reinterpret_cast<const float4*>(vh + static_cast<long long>(k0 + r) * D)[c];
-      }
-      reinterpret_cast<float4*>(Ks + r * KS)[c] = kv;
-      reinterpret_cast<float4*>(Vs + r * D)[c] = vv;
-    }
-    __syncthreads();
+  const int ntiles_cta = kend > kbeg ? (kend - kbeg + kBN - 1) / kBN : 0;
+  // group 0 takes the first ceil(n / 2) tiles, group 1 the rest
+  const int n0 = (ntiles_cta + 1) / 2;
+  const int tbeg = grp == 0 ? 0 : n0;
+  const int ntiles = grp == 0 ? n0 : ntiles_cta - n0;
+  const int bar_id = 1 + grp;  // the group's named barrier (barrier 0 is __syncthreads)
 
-    // scores of the warp's four rows against this lane's key
-    const int key = k0 + lane;
-    float dot[kRowsPerWarp];
-#pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) dot[r] = 0.f;
-    const float* kr = Ks + lane * KS;
-    for (int d = 0; d < D; d += 4) {
-      const float4 c = *reinterpret_cast<const float4*>(kr + d);
-#pragma unroll
-      for (int r = 0; r < kRowsPerWarp; ++r) {
-        const float4 a = *reinterpret_cast<const float4*>(qw_rows + r * D + d);
-        dot[r] = fmaf(a.x, c.x, dot[r]);
-        dot[r] = fmaf(a.y, c.y, dot[r]);
-        dot[r] = fmaf(a.z, c.z, dot[r]);
-        dot[r] = fmaf(a.w, c.w, dot[r]);
-      }
+  // K and V rows [k0, k0 + kBN) into buffer `buf`; rows past Nk are zero-filled
+  auto load_tile = [&](int k0, int buf) {
+    float* kd = Ks + buf * kBN * KS;
+    float* vd = Vs + buf * kBN * D;
+    for (int i = gtid; i < kBN * D4; i += kGroupWarps * 32) {
+      const int r = i / D4, c = i - r * D4;
+      const bool ok = k0 + r < Nk;
+      const long long src = static_cast<long long>(ok ? k0 + r : 0) * D + 4 * c;
+      cp_async16(kd + r * KS + 4 * c, kh + src, ok);
+      cp_async16(vd + r * D + 4 * c, vh + src, ok);
     }
-    // levels 1-2 per row: running max and sum in base 2, the output rescaled
+  };
+  for (int i = threadIdx.x; i < kBM * D4; i += kWarps * 32) {
+    const int r = i / D4, c = i - r * D4;
+    const bool ok = q0 + r < Nq;
+    cp_async16(Qs + r * KS + 4 * c, qh + static_cast<long long>(ok ? q0 + r : 0) * D + 4 * c, ok);
+  }
+  cp_async_commit();
+  if (ntiles > 0) load_tile(kbeg + tbeg * kBN, 0);
+  cp_async_commit();
+  cp_async_wait<1>();  // this thread's Q rows have landed
+  __syncthreads();     // every thread's have
+
+  float m[4], l[4], acc[4][NC][4];
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) {
-      const int qi = q0 + warp * kRowsPerWarp + r;
-      const bool visible = key < Nk && (!causal || key <= qi) && (window <= 0 || key > qi - window);
-      const float s2 = visible ? fmaf(slope2, static_cast<float>(key - qi), dot[r] * sl2) : -INFINITY;
-      const float m_new = fmaxf(m[r], warp_max(s2));
+  for (int i = 0; i < 4; ++i) {
+    m[i] = -INFINITY;
+    l[i] = 0.f;
+#pragma unroll
+    for (int c = 0; c < NC; ++c)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[i][c][e] = 0.f;
+  }
+  const float slope2 = alibi ? __ldg(alibi + h) * kLog2e : 0.f;
+  const float* qw = Qs + (wr * kRowsW + rg) * KS;  // row rg + 4i at qw + 4i KS
+  float* pw = Ps + warp * kRowsW * kPS;
+  const int row0 = q0 + wr * kRowsW + rg;          // query index of row i: row0 + 4i
+
+  for (int t = 0; t < ntiles; ++t) {
+    const int k0 = kbeg + (tbeg + t) * kBN, buf = t & 1;
+    if (t + 1 < ntiles) load_tile(k0 + kBN, buf ^ 1);
+    cp_async_commit();
+    cp_async_wait<1>();  // everything but the group just committed has landed
+    group_barrier(bar_id);
+
+    // S = Q K^T: rows rg + 4i, keys g + 8j of the tile
+    const float* kt = Ks + buf * kBN * KS + g * KS;
+    float s[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
+#pragma unroll
+    for (int d = 0; d < D; d += 4) {
+      float4 a[4], c[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4*>(qw + 4 * i * KS + d);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) c[j] = *reinterpret_cast<const float4*>(kt + 8 * j * KS + d);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          s[i][j] = fmaf(a[i].x, c[j].x, s[i][j]);
+          s[i][j] = fmaf(a[i].y, c[j].y, s[i][j]);
+          s[i][j] = fmaf(a[i].z, c[j].z, s[i][j]);
+          s[i][j] = fmaf(a[i].w, c[j].w, s[i][j]);
+        }
+    }
+    // levels 1-2 per row: running max and sum in base 2, the output rescaled.
+    // A tile whose keys every row of the warp sees needs no per-key test.
+    const int wq0 = row0 - rg, wq1 = wq0 + kRowsW - 1;  // the warp's first and last query rows
+    const bool interior = k0 + kBN <= Nk && (!causal || k0 + kBN - 1 <= wq0) && (window <= 0 || k0 > wq1 - window);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int qi = row0 + 4 * i;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int key = k0 + g + 8 * j;
+        const bool visible =
+            interior || (key < Nk && (!causal || key <= qi) && (window <= 0 || key > qi - window));
+        s[i][j] = visible ? fmaf(slope2, static_cast<float>(key - qi), s[i][j] * sl2) : -INFINITY;
+        mx = fmaxf(mx, s[i][j]);
+      }
+      const float m_new = fmaxf(m[i], group_max(mx));
       const float m_use = m_new == -INFINITY ? 0.f : m_new;  // no visible key for this row yet
-      const float alpha = exp2f(m[r] - m_use);                 // 0 when m was -inf
-      const float p = exp2f(s2 - m_use);                       // 0 for masked keys
-      l[r] = fmaf(l[r], alpha, warp_sum(p));
+      const float alpha = exp2f(m[i] - m_use);                 // 0 when m was -inf
+      float ps = 0.f;
 #pragma unroll
-      for (int c = 0; c < DC; ++c) acc[r][c] *= alpha;
-      m[r] = m_new;
-      pw[r * kBN + lane] = p;
+      for (int j = 0; j < 4; ++j) {
+        const float p = exp2f(s[i][j] - m_use);  // 0 for masked keys
+        ps += p;
+        pw[(rg + 4 * i) * kPS + g + 8 * j] = p;
+      }
+      l[i] = fmaf(l[i], alpha, group_sum(ps));
+#pragma unroll
+      for (int c = 0; c < NC; ++c)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[i][c][e] *= alpha;
+      m[i] = m_new;
     }
     __syncwarp();
-    // level 3: acc += P V, four keys of every row per broadcast load
+    // level 3: acc += P V over the tile's keys, four at a time
+    const float* vt = Vs + buf * kBN * D;
     for (int j = 0; j < kBN; j += 4) {
-      float4 pr[kRowsPerWarp];
+      float4 pr[4];
 #pragma unroll
-      for (int r = 0; r < kRowsPerWarp; ++r) pr[r] = *reinterpret_cast<const float4*>(pw + r * kBN + j);
+      for (int i = 0; i < 4; ++i) pr[i] = *reinterpret_cast<const float4*>(pw + (rg + 4 * i) * kPS + j);
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
-        const float* vr = Vs + (j + jj) * D;
+        const float* vr = vt + (j + jj) * D;
 #pragma unroll
-        for (int c = 0; c < DC; ++c) {
-          const int d = lane + 32 * c;
-          const float vv = d < D ? vr[d] : 0.f;
+        for (int c = 0; c < NC; ++c) {
+          const int d = 4 * g + 32 * c;
+          const float4 vv = d < D ? *reinterpret_cast<const float4*>(vr + d) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-          for (int r = 0; r < kRowsPerWarp; ++r) {
-            const float pj = jj == 0 ? pr[r].x : (jj == 1 ? pr[r].y : (jj == 2 ? pr[r].z : pr[r].w));
-            acc[r][c] = fmaf(pj, vv, acc[r][c]);
+          for (int i = 0; i < 4; ++i) {
+            const float pj = jj == 0 ? pr[i].x : (jj == 1 ? pr[i].y : (jj == 2 ? pr[i].z : pr[i].w));
+            acc[i][c][0] = fmaf(pj, vv.x, acc[i][c][0]);
+            acc[i][c][1] = fmaf(pj, vv.y, acc[i][c][1]);
+            acc[i][c][2] = fmaf(pj, vv.z, acc[i][c][2]);
+            acc[i][c][3] = fmaf(pj, vv.w, acc[i][c][3]);
           }
         }
       }
     }
-    __syncwarp();  // the warp has read its probabilities before the next tile writes them
+    group_barrier(bar_id);  // the group is done with this buffer before the next prefetch overwrites it
+  }
+  cp_async_wait<0>();
+
+  // Merge the two key groups (RedFuser, Figure 13): group 1 leaves its state
+  // in its own K / V buffers and P rows, lane for lane; group 0 combines
+  // m = max(m0, m1), l = l0 a0 + l1 a1, acc = acc0 a0 + acc1 a1 with
+  // a_g = 2^(m_g - m).
+  float* xacc = Qs + kBM * KS + 2 * kBN * KS;  // group 1's K buffers: [4 warps][32 lanes][4][NC][4]
+  float* xml = Ps + kGroupWarps * kRowsW * kPS;  // group 1's P rows: [4 warps][32 lanes][8]
+  if (grp == 1) {
+    float* xa = xacc + (wr * 32 + lane) * (16 * NC);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int c = 0; c < NC; ++c)
+        *reinterpret_cast<float4*>(xa + (i * NC + c) * 4) = make_float4(acc[i][c][0], acc[i][c][1], acc[i][c][2], acc[i][c][3]);
+    float* xm = xml + (wr * 32 + lane) * 8;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      xm[i] = m[i];
+      xm[4 + i] = l[i];
+    }
+  }
+  __syncthreads();
+  if (grp == 1) return;
+  {
+    const float* xa = xacc + (wr * 32 + lane) * (16 * NC);
+    const float* xm = xml + (wr * 32 + lane) * 8;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float m1 = xm[i], l1 = xm[4 + i];
+      const float mm = fmaxf(m[i], m1);
+      const float mu = mm == -INFINITY ? 0.f : mm;
+      const float a0 = exp2f(m[i] - mu), a1 = exp2f(m1 - mu);
+      l[i] = l[i] * a0 + l1 * a1;
+      m[i] = mm;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        const float4 x = *reinterpret_cast<const float4*>(xa + (i * NC + c) * 4);
+        acc[i][c][0] = fmaf(acc[i][c][0], a0, x.x * a1);
+        acc[i][c][1] = fmaf(acc[i][c][1], a0, x.y * a1);
+        acc[i][c][2] = fmaf(acc[i][c][2], a0, x.z * a1);
+        acc[i][c][3] = fmaf(acc[i][c][3], a0, x.w * a1);
+      }
+    }
   }
 
   constexpr float kLn2 = 0.6931471805599453f;
 #pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) {
-    const int qi = q0 + warp * kRowsPerWarp + r;
+  for (int i = 0; i < 4; ++i) {
+    const int qi = row0 + 4 * i;
     if (qi >= Nq) continue;
     const long long orow = (static_cast<long long>(b) * Hq + h) * Nq + qi;
-    const bool live = l[r] > 0.f;
-    const float inv = live ? 1.0f / l[r] : 0.f;
+    const bool live = l[i] > 0.f;
+    const float inv = live ? 1.0f / l[i] : 0.f;
 #pragma unroll
-    for (int c = 0; c < DC; ++c) {
-      const int d = lane + 32 * c;
-      if (d < D) o[orow * D + d] = acc[r][c] * inv;
+    for (int c = 0; c < NC; ++c) {
+      const int d = 4 * g + 32 * c;
+      if (d < D)
+        *reinterpret_cast<float4*>(o + orow * D + d) =
+            make_float4(acc[i][c][0] * inv, acc[i][c][1] * inv, acc[i][c][2] * inv, acc[i][c][3] * inv);
     }
-    if (lse && lane == 0) lse[orow] = live ? (m[r] + log2f(l[r])) * kLn2 : -INFINITY;
+    if (lse && g == 0) lse[orow] = live ? (m[i] + log2f(l[i])) * kLn2 : -INFINITY;
   }
 }
 
@@ -176,14 +318,26 @@ cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, floa
                             unsigned* status, cudaStream_t s) {
   const dim3 grid((Nq + kBM - 1) / kBM, Hq, B);
   if (B > 65535 || Hq > 65535) return cudaErrorInvalidConfiguration;
-  const size_t smem = sizeof(float) * (kBM * D + kBN * (D + 4) + kBN * D + kWarps * kRowsPerWarp * kBN);
-  const int dc = (D + 31) / 32;
-  switch (dc) {
-    case 1: attn_f32_kernel<1><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi, status); break;
-    case 2: attn_f32_kernel<2><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi, status); break;
-    case 3: attn_f32_kernel<3><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi, status); break;
-    default: attn_f32_kernel<4><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal, window, alibi, status); break;
+  const int KS = padded_stride(D);
+  const size_t smem =
+      sizeof(float) * (static_cast<size_t>(kBM) * KS + kGroups * 2 * kBN * (KS + D) + kWarps * kRowsW * kPS);
+  const int nc = (D + 31) / 32;
+  const bool fixed = D == 32 * nc;  // 32, 64, 96, 128: the compile-time instances
+#define RF_F32_LAUNCH(NC, DC)                                                                               \
+  do {                                                                                                      \
+    cudaError_t e = cudaFuncSetAttribute(attn_f32_kernel<NC, DC>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                         static_cast<int>(smem));                                           \
+    if (e != cudaSuccess) return e;                                                                         \
+    attn_f32_kernel<NC, DC><<<grid, kWarps * 32, smem, s>>>(q, k, v, o, lse, Hq, Hkv, Nq, Nk, D, scale, causal, \
+                                                            window, alibi, status);                         \
+  } while (0)
+  switch (nc) {
+    case 1: if (fixed) RF_F32_LAUNCH(1, 32); else RF_F32_LAUNCH(1, 0); break;
+    case 2: if (fixed) RF_F32_LAUNCH(2, 64); else RF_F32_LAUNCH(2, 0); break;
+    case 3: if (fixed) RF_F32_LAUNCH(3, 96); else RF_F32_LAUNCH(3, 0); break;
+    default: if (fixed) RF_F32_LAUNCH(4, 128); else RF_F32_LAUNCH(4, 0); break;
   }
+#undef RF_F32_LAUNCH
   return cudaGetLastError();
 }
 

@@ -34,6 +34,10 @@ def test_tiny_workload(rf):
     (1, 8, 1, 100, 100, 100, True),
     (3, 2, 1, 17, 5, 36, False),
     (1, 1, 1, 300, 300, 128, True),
+    (1, 2, 1, 200, 333, 64, False),   # several 64-row blocks and 32-key tiles, both ragged
+    (1, 1, 1, 129, 129, 32, True),    # one output group per lane, a one-row last block
+    (1, 3, 3, 65, 300, 96, False),    # three output groups per lane
+    (2, 2, 2, 64, 64, 64, True),      # exactly one block and two tiles
 ])
 def test_shapes(rf, B, Hq, Hkv, Nq, Nk, D, causal):
     q, k, v = inputs.attn_inputs(B, Hq, Hkv, Nq, Nk, D, "f32", seed=Nq + D)
