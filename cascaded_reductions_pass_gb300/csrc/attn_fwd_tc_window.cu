@@ -357,8 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = warp_wait(&bars->s_full[t], cnt & 1))) break;
         tc_fence_after();
         uint32_t s[kBN];
-#pragma unroll
-        for (int i = 0; i < kBN / 32; ++i) tc_ld32(tS + 32 * i, s + 32 * i);
+        tc_ld128(tS, s);  // the row's 128 scores in one load
         tc_wait_ld();
         tc_fence_before();  // S_t may be overwritten by the next S_t now
         mbar_arrive(&bars->s_free[t]);
@@ -409,8 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = warp_wait(&bars->pv_done[t], (cnt - 1) & 1))) break;
           tc_fence_after();
         }
-#pragma unroll
-        for (int cc = 0; cc < kBN / 16; ++cc) tc_st8(tP + 8 * cc, pk + 8 * cc);
+        tc_st64(tP, pk);  // P of the row in one store
         l_run = fmaf(l_run, alpha, tsum);
         // level 3 correction: rescale O in TMEM when some row's max moved
         if (jt > 0 && __any_sync(0xffffffffu, need)) {
