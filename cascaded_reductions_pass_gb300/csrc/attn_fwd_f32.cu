@@ -260,7 +260,8 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const float* __re
     for (int i = 0; i < 4; ++i)
 #pragma unroll
       for (int c = 0; c < NC; ++c)
-        *reinterpret_cast<float4*>(xa + (i * NC + c) * 4) = make_float4(acc[i][c][0], acc[i][c][1], acc[i][c][2], acc[i][c][3]);
+        *reinterpret_cast<float4*>(xa + (i * NC + c) * 4) =
+            make_float4(acc[i][c][0], acc[i][c][1], acc[i][c][2], acc[i][c][3]);
     float* xm = xml + (wr * 32 + lane) * 8;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {

@@ -53,3 +53,16 @@ def test_constant_v_and_softmax_sum(rf):
     v = torch.ones(1, 1, 40, 64)
     o, _ = run(rf, q, k, v, 0.125, True)
     np.testing.assert_allclose(o.numpy(), 1.0, rtol=0, atol=2e-6)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_full_workload_b1_h8_n2048(rf, causal):
+    """The B=1 H=8 N=2048 D=64 workload the bench times (64 key tiles per 64-row
+    block, split 32 / 32 between the two warp groups), every output against the
+    oracle; causal too, where the two halves of a block's keys differ in length."""
+    w = inputs.WORKLOADS["attn_f32_d64_n2048"]
+    q, k, v = inputs.make(w)
+    o, lse = run(rf, q, k, v, 0.125, causal)
+    ro, rl = oracle.attention(q, k, v, 0.125, causal)
+    check32(o, ro, f"B=1 H=8 N=2048 causal={causal}")
+    check_lse(lse, rl, tol=1e-5 * max(1, np.abs(rl).max()))
