@@ -133,7 +133,8 @@ struct AttnTailRows {
 template <Dt DT, int D, int MASK, bool ALIBI, int ROPE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                   const __grid_constant__ CUtensorMap tv, uint16_t* __restrict__ o, float* __restrict__ lse,
+                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                   float* __restrict__ lse,
                    int Hq, int Hkv, int Nq, int Nk, int BH, int nqt, float sl2, int window,
                    const float* __restrict__ alibi, unsigned* status, int n_full, int n_split,
                    float* __restrict__ o_part, float* __restrict__ lse_part,
@@ -681,9 +682,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (row_ok && in_ws) lse_part[g * n_split + split] = (m_run + log2f(l_run)) * kLn2;
       } else {
+        // The warp's 32 rows of O are contiguous in memory: they are staged in
+        // Q_t's shared-memory tile (free now: every S_t has completed), in the
+        // 128-byte swizzle Q arrived in, and written by one TMA store per
+        // 64-column box (rows past Nq are clipped); a per-thread store of each
+        // row touched 32 lines per instruction.
         const bool in_o = RF_INB(bh < BH && (!row_ok || (row >= 0 && row < Nq)), status);
-        uint4* orow =
-            reinterpret_cast<uint4*>(o + (static_cast<long long>(bh) * Nq + (row_ok ? row : 0)) * D);
+        uint8_t* ob = sQ + t * C::kQBytes + qw * 32 * 128;  // row `lane` of the warp at ob + lane * 128
 #pragma unroll
         for (int i = 0; i < D / 32; ++i) {
           uint32_t ov[32];
@@ -693,11 +698,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e)
             pk[e] = Pack<DT>::pack2(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
-          if (row_ok && in_o) {
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              orow[i * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          for (int v4 = 0; v4 < 4; ++v4) {  // 16-byte chunk gc of the row: box gc / 8, chunk gc mod 8
+            const int gc = 4 * i + v4;
+            *reinterpret_cast<uint4*>(ob + (gc >> 3) * (kBM * 128) + lane * 128 + ((((gc & 7) ^ lane) & 7) << 4)) =
+                make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
           }
+        }
+        fence_proxy_async_smem();  // the staged rows are visible to the TMA store
+        __syncwarp();
+        const int wrow = row - lane;  // the warp's first row
+        if (lane == 0 && wrow < Nq && in_o) {
+#pragma unroll
+          for (int bx = 0; bx < D / 64; ++bx) tma_store_3d(&to, ob + bx * (kBM * 128), bx * 64, wrow, bh);
+          tma_store_commit();
+          tma_store_wait_all();  // the stores have landed before the CTA exits
         }
         if (row_ok && in_o && lse) lse[static_cast<long long>(bh) * Nq + row] = (m_run + log2f(l_run)) * kLn2;
       }
@@ -760,9 +775,10 @@ template <Dt DT, int D, int MASK, bool ALIBI, int ROPE>
 cudaError_t launch_cfg(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                        int Nq, int Nk, float scale, int window, const float* alibi, unsigned* status,
                        const TailPlan& plan, void* ws, const AttnRope& rp, cudaStream_t s) {
-  alignas(64) CUtensorMap tq, tk, tv;
+  alignas(64) CUtensorMap tq, tk, tv, to;
   cudaError_t err = cudaSuccess;
   if (!encode_tma_3d_16bit(&tq, q, D, Nq, uint64_t(B) * Hq, kBM, &err)) return err;
+  if (!encode_tma_3d_16bit(&to, o, D, Nq, uint64_t(B) * Hq, 32, &err)) return err;  // one warp's rows
   if (!encode_tma_3d_16bit(&tk, k, D, Nk, uint64_t(B) * Hkv, kBN, &err)) return err;
   if (!encode_tma_3d_16bit(&tv, v, D, Nk, uint64_t(B) * Hkv, kBN, &err)) return err;
   const int nqt = (Nq + 2 * kBM - 1) / (2 * kBM);
@@ -789,7 +805,7 @@ cudaError_t launch_cfg(const void* q, const void* k, const void* v, void* o, flo
   float* lse_part = split ? reinterpret_cast<float*>(static_cast<char*>(ws) + tail_o_bytes(plan, D)) : nullptr;
   const long long n_full = split ? plan.n_full : grid;
   const long long ctas = split ? plan.n_full + static_cast<long long>(plan.tail) * plan.n_split : grid;
-  kern<<<static_cast<unsigned>(ctas), kThreads, smem, s>>>(tq, tk, tv, static_cast<uint16_t*>(o), lse, Hq, Hkv, Nq,
+  kern<<<static_cast<unsigned>(ctas), kThreads, smem, s>>>(tq, tk, tv, to, lse, Hq, Hkv, Nq,
                                                            Nk, B * Hq, nqt, scale * kLog2e, window, alibi, status,
                                                            static_cast<int>(n_full), split ? plan.n_split : 1,
                                                            o_part, lse_part, rope, rp.pos, batch_major);

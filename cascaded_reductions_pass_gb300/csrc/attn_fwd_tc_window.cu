@@ -41,6 +41,7 @@ constexpr int kWQBytes = kBM * kWD * 2;      // one query tile
 constexpr int kWKVBytes = kBN * kWD * 2;     // one K or V tile
 constexpr int kWStages = 3;                  // K/V ring depth
 constexpr int kWTiles = 2 * 2 * kWQBytes + 2 * kWStages * kWKVBytes;  // Q [tile][buffer], K ring, V ring
+constexpr int kWOStage = 8 * 32 * kWD * 2;   // O staging: 32 rows x 128 B per softmax warp
 constexpr int kWOCol = 2 * kBN;              // O0 at 256, O1 at 320
 constexpr int kWPCol = 2 * kBN + 2 * kWD;    // P0 at 384, P1 at 448
 constexpr int kMaxItems = 1024;              // items per CTA (the grid widens beyond that)
@@ -88,7 +89,8 @@ __device__ __forceinline__ bool aborted(const WinBars* bars) {
 template <Dt DT, bool ALIBI>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_window_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                          const __grid_constant__ CUtensorMap tv, uint16_t* __restrict__ o, float* __restrict__ lse,
+                          const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                          float* __restrict__ lse,
                           int Hq, int Hkv, int Nq, float sl2, const float* __restrict__ alibi, unsigned* status,
                           const WinSched sc) {
   constexpr int S = kWStages;
@@ -98,7 +100,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sQ = smem;  // query tile t, buffer qb at sQ + (2 t + qb) * kWQBytes
   uint8_t* sK = sQ + 4 * kWQBytes;
   uint8_t* sV = sK + S * kWKVBytes;
-  WinBars* bars = reinterpret_cast<WinBars*>(sV + S * kWKVBytes);
+  uint8_t* sO = sV + S * kWKVBytes;  // O staging of softmax warp w at sO + (w - 4) * 4 KB (1 KB aligned)
+  WinBars* bars = reinterpret_cast<WinBars*>(sO + kWOStage);
   WinItem* items =
       reinterpret_cast<WinItem*>(reinterpret_cast<uint8_t*>(bars) + ((sizeof(WinBars) + 15) & ~size_t(15)));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -436,12 +439,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (jhi <= jlo) continue;
       if (!(ok = warp_wait(&bars->o_final[t], nfin & 1))) break;
       ++nfin;
-      // epilogue: O / l in the output dtype, LSE in natural log
+      // epilogue: O / l in the output dtype, LSE in natural log.  The warp's 32
+      // rows (4 KB, contiguous in O) go through its staging buffer in the
+      // 128-byte swizzle of the O tensor map, and one TMA store writes them
+      // (rows past Nq are clipped): a per-thread store of each 128-byte row
+      // touched 32 lines per instruction.
       tc_fence_after();
       const float inv = 1.0f / l_run;
       const bool row_ok = row < Nq;
       const bool in_o = RF_INB(bh < sc.BH && row >= 0, status);
-      uint4* orow = reinterpret_cast<uint4*>(o + (static_cast<long long>(bh) * Nq + (row_ok ? row : 0)) * kWD);
+      uint8_t* ob = sO + (warp - 4) * (32 * kWD * 2);
+      if (lane == 0) tma_store_wait_read();  // the previous item's store has read the buffer
+      __syncwarp();
 #pragma unroll
       for (int i = 0; i < kWD / 32; ++i) {
         uint32_t ov[32];
@@ -451,11 +460,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           pk[e] = Pack<DT>::pack2(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
-        if (row_ok && in_o) {
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            orow[i * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-        }
+        for (int v4 = 0; v4 < 4; ++v4)  // 16-byte chunk 4 i + v4 of row `lane`, at chunk (4 i + v4) ^ (lane mod 8)
+          *reinterpret_cast<uint4*>(ob + lane * 128 + ((((4 * i + v4) ^ lane) & 7) << 4)) =
+              make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+      }
+      fence_proxy_async_smem();  // the staged rows are visible to the TMA store
+      __syncwarp();
+      const int wrow = row - lane;  // the warp's first row
+      if (lane == 0 && wrow < Nq && in_o) {
+        tma_store_3d(&to, ob, 0, wrow, bh);
+        tma_store_commit();
       }
       if (row_ok && in_o && lse) lse[static_cast<long long>(bh) * Nq + row] = (m_run + log2f(l_run)) * kLn2;
       // O_t has been read (tcgen05.ld waited); the fence before this thread's
@@ -465,6 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) atomicOr(status, kStatusTimeout);
       bars->abort = 1;
     }
+    if (lane == 0) tma_store_wait_all();  // every O store of this warp has landed
   }
 
   tc_fence_before();
@@ -479,9 +495,10 @@ template <Dt DT, bool ALIBI>
 cudaError_t launch_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                           int Nq, int Nk, float scale, int window, const float* alibi, unsigned* status, int sms,
                           cudaStream_t s) {
-  alignas(64) CUtensorMap tq, tk, tv;
+  alignas(64) CUtensorMap tq, tk, tv, to;
   cudaError_t err = cudaSuccess;
   if (!encode_tma_3d_16bit(&tq, q, kWD, Nq, uint64_t(B) * Hq, kBM, &err)) return err;
+  if (!encode_tma_3d_16bit(&to, o, kWD, Nq, uint64_t(B) * Hq, 32, &err)) return err;  // one warp's rows
   if (!encode_tma_3d_16bit(&tk, k, kWD, Nk, uint64_t(B) * Hkv, kBN, &err)) return err;
   if (!encode_tma_3d_16bit(&tv, v, kWD, Nk, uint64_t(B) * Hkv, kBN, &err)) return err;
   const int nqt = (Nq + 2 * kBM - 1) / (2 * kBM);
@@ -497,12 +514,12 @@ cudaError_t launch_window(const void* q, const void* k, const void* v, void* o, 
   long long ctas = sms > 0 && sms < n_items ? sms : n_items;
   const long long min_ctas = (n_items + kMaxItems - 1) / kMaxItems;
   if (ctas < min_ctas) ctas = min_ctas;
-  const int smem = kWTiles + 1024 + static_cast<int>((sizeof(WinBars) + 15) & ~size_t(15)) +
+  const int smem = kWTiles + kWOStage + 1024 + static_cast<int>((sizeof(WinBars) + 15) & ~size_t(15)) +
                    kMaxItems * static_cast<int>(sizeof(WinItem)) + 64;
   auto kern = attn_tc_window_kernel<DT, ALIBI>;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  kern<<<static_cast<unsigned>(ctas), kThreads, smem, s>>>(tq, tk, tv, static_cast<uint16_t*>(o), lse, Hq, Hkv, Nq,
+  kern<<<static_cast<unsigned>(ctas), kThreads, smem, s>>>(tq, tk, tv, to, lse, Hq, Hkv, Nq,
                                                            scale * kLog2e, alibi, status, sc);
   return cudaGetLastError();
 }

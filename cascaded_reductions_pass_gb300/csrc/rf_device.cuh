@@ -310,6 +310,25 @@ __device__ __forceinline__ void tma_load_3d_elect(void* dst, const void* tmap, u
       "l"(tmap), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+// 3-D tiled store of a shared-memory box (coordinates innermost first, none
+// negative; rows past the tensor are clipped), tracked by this thread's bulk
+// group.  The box's shared-memory writes must be made visible to the async
+// proxy first (fence_proxy_async_smem).
+__device__ __forceinline__ void tma_store_3d(const void* tmap, const void* src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(tmap),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// This thread's committed stores have read their shared-memory source.
+__device__ __forceinline__ void tma_store_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// This thread's committed stores are complete.
+__device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 // Bounded wait with one outcome for the whole warp.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, unsigned parity) {
   const bool ok = mbar_wait(bar, parity);
