@@ -211,6 +211,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars->abort = 0;
     fence_mbar_init();
   }
+  // The producer warp (whose lane 0 initialised the barriers) starts the copies
+  // that need no wait, Q and the first ring stages, before the CTA-wide barrier:
+  // they overlap the TMEM allocation and the barrier itself.
+  const int n_early = min(S, n_load);
+  if (warp == 0) {
+    __syncwarp();
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
+    if (lane == 0) (void)RF_INB(bh < BH && r0 < Nq && kv_plane < (BH / Hq) * Hkv && lo0 >= 0 && nt1 <= n_kv, status);
+    mbar_expect_tx_elect(&bars->q_full, 2 * C::kQBytes);
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int bx = 0; bx < D / 64; ++bx)
+        tma_load_3d_elect(sQ + t * C::kQBytes + bx * (kBM * 128), &tq, &bars->q_full, bx * 64, r0 + t * kBM, bh);
+    for (int jj = 0; jj < n_early; ++jj) {  // ring slot jj holds key tile lo0 + jj
+      const int key0 = (lo0 + jj) * kBN;
+      if (lane == 0) (void)RF_INB(key0 < Nk, status);
+      mbar_expect_tx_elect(&bars->k_full[jj], C::kSepP ? 2 * C::kKVBytes : C::kKVBytes);
+#pragma unroll
+      for (int bx = 0; bx < D / 64; ++bx)
+        tma_load_3d_elect(sK + jj * C::kKVBytes + bx * (kBN * 128), &tk, &bars->k_full[jj], bx * 64, key0, kv_plane);
+      uint64_t* vbar = C::kSepP ? &bars->k_full[jj] : &bars->v_full[jj];  // V rides on K's barrier at D = 64
+      if (!C::kSepP) mbar_expect_tx_elect(vbar, C::kKVBytes);
+#pragma unroll
+      for (int bx = 0; bx < D / 64; ++bx)
+        tma_load_3d_elect(sV + jj * C::kKVBytes + bx * (kBN * 128), &tv, vbar, bx * 64, key0, kv_plane);
+    }
+  }
   if (warp == 1) {
     tc_alloc(&bars->tmem_base, kTmemCols);
     tc_relinquish();
@@ -227,19 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_dec<kRegsCtl>();
     if (warp == 0) {
       // ---------------------------------------------------------- TMA producer (whole warp, one lane issues)
-      tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tk);
-      tma_prefetch_desc(&tv);
-      if (lane == 0) (void)RF_INB(bh < BH && r0 < Nq && kv_plane < (BH / Hq) * Hkv && lo0 >= 0 && nt1 <= n_kv, status);
-      mbar_expect_tx_elect(&bars->q_full, 2 * C::kQBytes);
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-#pragma unroll
-        for (int bx = 0; bx < D / 64; ++bx)
-          tma_load_3d_elect(sQ + t * C::kQBytes + bx * (kBM * 128), &tq, &bars->q_full, bx * 64, r0 + t * kBM, bh);
-      int issued_k = 0, issued_v = 0;
+      // Q and key tiles [0, n_early) were issued before the CTA-wide barrier.
+      int issued_k = n_early, issued_v = C::kSepP ? 0 : n_early;
       bool ok = true;
-      for (int jj = 0; jj < n_load; ++jj) {  // ring slot jj holds key tile lo0 + jj
+      for (int jj = n_early; jj < n_load; ++jj) {  // ring slot jj % S holds key tile lo0 + jj
         const int st = jj % S, key0 = (lo0 + jj) * kBN;
         if (lane == 0) (void)RF_INB(key0 < Nk, status);
         if (jj >= S && !(ok = mbar_wait_warp(&bars->k_empty[st], ((jj / S) - 1) & 1))) break;
@@ -712,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int bx = 0; bx < D / 64; ++bx) tma_store_3d(&to, ob + bx * (kBM * 128), bx * 64, wrow, bh);
           tma_store_commit();
-          tma_store_wait_all();  // the stores have landed before the CTA exits
+          tma_store_wait_read();  // Q_t's tile has been read before the CTA exits; the writes finish on their own
         }
         if (row_ok && in_o && lse) lse[static_cast<long long>(bh) * Nq + row] = (m_run + log2f(l_run)) * kLn2;
       }

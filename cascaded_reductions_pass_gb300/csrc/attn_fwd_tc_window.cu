@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) atomicOr(status, kStatusTimeout);
       bars->abort = 1;
     }
-    if (lane == 0) tma_store_wait_all();  // every O store of this warp has landed
+    if (lane == 0) tma_store_wait_read();  // the staging buffer has been read before the CTA exits
   }
 
   tc_fence_before();

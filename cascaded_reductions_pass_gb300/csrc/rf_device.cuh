@@ -320,12 +320,12 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, const void* src, 
                : "memory");
 }
 __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// This thread's committed stores have read their shared-memory source.
+// This thread's committed stores have read their shared-memory source (the
+// buffer may be reused or released; their global writes complete on their own
+// and are visible when the kernel has finished).
 __device__ __forceinline__ void tma_store_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
-// This thread's committed stores are complete.
-__device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
