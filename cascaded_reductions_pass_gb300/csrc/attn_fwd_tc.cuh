@@ -73,6 +73,10 @@
 #include <cuda.h>
 #include <math.h>
 
+#ifndef RF_Q_PREFETCH
+#define RF_Q_PREFETCH 1
+#endif
+
 #include "attn_tc_common.cuh"
 #include "lse_merge.cuh"
 #include "rf_device.cuh"
@@ -138,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    int Hq, int Hkv, int Nq, int Nk, int BH, int nqt, float sl2, int window,
                    const float* __restrict__ alibi, unsigned* status, int n_full, int n_split,
                    float* __restrict__ o_part, float* __restrict__ lse_part,
-                   const __grid_constant__ RopeParams rope, int rope_pos, int batch_major) {
+                   const __grid_constant__ RopeParams rope, int rope_pos, int batch_major, int prefetch_stride) {
   constexpr bool CAUSAL = MASK >= 1;
   constexpr bool kSpec = D == 64 && MASK == 0 && !ALIBI;
   using C = Cfg<D>;
@@ -162,18 +166,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool piece = MASK == 0 && id >= n_full;
   const int unit = piece ? n_full + (id - n_full) / n_split : id;
   const int split = piece ? (id - n_full) % n_split : 0;
+  // unit -> query-tile pair c and batch*head bh
+  auto coords = [&](int u, int& cc, int& bhh) {
+    if (CAUSAL && batch_major) {
+      // Batch-major order (longest units first within each batch): only one
+      // batch's K and V tiles are live in L2 at a time, for when every head's K
+      // and V together would not stay there.
+      const int per_b = Hq * nqt;
+      const int bb = u / per_b, r = u - bb * per_b;
+      cc = nqt - 1 - r / Hq;
+      bhh = bb * Hq + (r - (r / Hq) * Hq);
+    } else {
+      unit_coords(u, BH, nqt, cc, bhh);
+    }
+  };
   int c, bh;
-  if (CAUSAL && batch_major) {
-    // Batch-major order (longest units first within each batch): only one
-    // batch's K and V tiles are live in L2 at a time, for when every head's K
-    // and V together would not stay there.
-    const int per_b = Hq * nqt;
-    const int bb = unit / per_b, r = unit - bb * per_b;
-    c = nqt - 1 - r / Hq;
-    bh = bb * Hq + (r - (r / Hq) * Hq);
-  } else {
-    unit_coords(unit, BH, nqt, c, bh);
-  }
+  coords(unit, c, bh);
   const int h = bh % Hq, b = bh / Hq;
   const int kv_plane = b * Hkv + h / (Hq / Hkv);
   const int r0 = c * 2 * kBM;
@@ -227,6 +235,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int bx = 0; bx < D / 64; ++bx)
         tma_load_3d_elect(sQ + t * C::kQBytes + bx * (kBM * 128), &tq, &bars->q_full, bx * 64, r0 + t * kBM, bh);
+    // With one CTA per SM, CTA id + prefetch_stride is about the one that takes
+    // this SM (or another) next: its Q tiles go to L2 now, so that its own
+    // first load, which nothing overlaps, does not wait on HBM.
+    const int nid = id + prefetch_stride;
+    if (prefetch_stride > 0 && nid < static_cast<int>(gridDim.x)) {
+      const int nunit = MASK == 0 && nid >= n_full ? n_full + (nid - n_full) / n_split : nid;
+      int nc, nbh;
+      coords(nunit, nc, nbh);
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int bx = 0; bx < D / 64; ++bx) tma_prefetch_l2_3d_elect(&tq, bx * 64, nc * 2 * kBM + t * kBM, nbh);
+    }
     for (int jj = 0; jj < n_early; ++jj) {  // ring slot jj holds key tile lo0 + jj
       const int key0 = (lo0 + jj) * kBN;
       if (lane == 0) (void)RF_INB(key0 < Nk, status);
@@ -829,7 +850,8 @@ cudaError_t launch_cfg(const void* q, const void* k, const void* v, void* o, flo
   kern<<<static_cast<unsigned>(ctas), kThreads, smem, s>>>(tq, tk, tv, to, lse, Hq, Hkv, Nq,
                                                            Nk, B * Hq, nqt, scale * kLog2e, window, alibi, status,
                                                            static_cast<int>(n_full), split ? plan.n_split : 1,
-                                                           o_part, lse_part, rope, rp.pos, batch_major);
+                                                           o_part, lse_part, rope, rp.pos, batch_major,
+                                                           RF_Q_PREFETCH ? device_sm_count() : 0);
   err = cudaGetLastError();
   if (err != cudaSuccess || !split) return err;
   const int rows = plan.tail * 2 * kBM;

@@ -329,6 +329,15 @@ __device__ __forceinline__ void tma_store_wait_read() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// 3-D tile of a tensor map fetched into L2 only (no shared memory, no
+// barrier); one elected lane of the warp issues it.
+__device__ __forceinline__ void tma_prefetch_l2_3d_elect(const void* tmap, int c0, int c1, int c2) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n\t}" ::"l"(tmap),
+      "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
 // Bounded wait with one outcome for the whole warp.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, unsigned parity) {
   const bool ok = mbar_wait(bar, parity);
