@@ -76,6 +76,9 @@
 #ifndef RF_Q_PREFETCH
 #define RF_Q_PREFETCH 1
 #endif
+#ifndef RF_MERGE_PDL
+#define RF_MERGE_PDL 1
+#endif
 
 #include "attn_tc_common.cuh"
 #include "lse_merge.cuh"
@@ -270,6 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  // The merge of a split tail (if any) may be scheduled once every CTA has
+  // started; it waits on the device for this grid to complete.
+  griddep_launch_dependents();
 
   // Register split: 128 x 80 (producer / MMA warpgroup) + 256 x 208 (softmax)
   // = 63,488 <= 384 x 168 registers granted at launch.
@@ -856,9 +862,21 @@ cudaError_t launch_cfg(const void* q, const void* k, const void* v, void* o, flo
   if (err != cudaSuccess || !split) return err;
   const int rows = plan.tail * 2 * kBM;
   const AttnTailRows map{static_cast<int>(plan.n_full), B * Hq, nqt, Nq};
-  lse_merge_kernel<DT><<<(rows + kMergeWarps - 1) / kMergeWarps, kMergeWarps * 32, 0, s>>>(
-      o_part, lse_part, o, lse, rows, plan.n_split, D, map, static_cast<long long>(B) * Hq * Nq, status);
-  return cudaGetLastError();
+  // Launched with programmatic stream serialisation: its launch overlaps the
+  // attention grid's last wave, and it waits on the device for that grid.
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(static_cast<unsigned>((rows + kMergeWarps - 1) / kMergeWarps));
+  lc.blockDim = dim3(kMergeWarps * 32);
+  lc.dynamicSmemBytes = 0;
+  lc.stream = s;
+  cudaLaunchAttribute la[1];
+  la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  la[0].val.programmaticStreamSerializationAllowed = RF_MERGE_PDL;
+  lc.attrs = la;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, lse_merge_kernel<DT, AttnTailRows>, static_cast<const float*>(o_part),
+                            static_cast<const float*>(lse_part), o, lse, rows, plan.n_split, D, map,
+                            static_cast<long long>(B) * Hq * Nq, status);
 }
 
 // One head dimension and rotary mode: the mask and ALiBi pick the instance

@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     fence_mbar_init();
   }
   __syncthreads();
+  griddep_launch_dependents();  // the merge may be scheduled once every split has started
 
   // Per-lane partial state (consumer warps): heads 2t, 2t+1 of the group.
   const int g = lane >> 2, t = lane & 3;

@@ -388,7 +388,7 @@ rf_status_t rf_attn_decode_splitkv(const void* q, const void* k_cache, const voi
                            "rf_attn_decode_splitkv(split)");
   if (r != RF_OK) return r;
   return launched(rf::launch_lse_merge(o_part, lse_part, o, lse, int(rows), num_splits, D,
-                                       static_cast<rf::Dt>(dtype), st, s),
+                                       static_cast<rf::Dt>(dtype), st, s, /*after_split=*/true),
                   "rf_attn_decode_splitkv(merge)");
 }
 

@@ -25,9 +25,12 @@ cudaError_t launch_rmsnorm(const void* x, const void* r, const void* gamma, void
 cudaError_t launch_xent(const void* logits, const long long* targets, float* loss, float* lse, void* grad, int rows,
                         int vocab, long long ignore_index, Dt dt, unsigned* status, cudaStream_t s);
 
-// log-sum-exp merge of split partials (lse_merge.cu)
+// log-sum-exp merge of split partials (lse_merge.cu); after_split: launched
+// right after the kernel that writes the partials, which lets it be scheduled
+// early (programmatic dependent launch; the merge waits for that kernel)
 cudaError_t launch_lse_merge(const float* o_part, const float* lse_part, void* o, float* lse,
-                             int rows, int splits, int D, Dt out_dt, unsigned* status, cudaStream_t s);
+                             int rows, int splits, int D, Dt out_dt, unsigned* status, cudaStream_t s,
+                             bool after_split = false);
 
 // exact fp32 SIMT attention forward (attn_fwd_f32.cu)
 cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, float* o, float* lse,
