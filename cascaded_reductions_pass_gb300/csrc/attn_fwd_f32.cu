@@ -18,7 +18,8 @@
 // 8 rg + g (row group rg < 4, column group g < 8) holds rows rg + 4i (i < 4)
 // of its warp, and
 //   S = Q K^T   the keys g + 8i' (i' < 4) of the tile: 16 scores per lane,
-//               64 FFMA per four Q and four K float4 loads;
+//               32 packed fma.f32x2 (64 products) per four Q and four K
+//               float4 loads;
 //   O += P V    the output columns 4g + 32c + e (c < NC, e < 4): 16 NC
 //               accumulators, 16 NC FFMA per key from one P and NC V float4.
 // Row max and row sum finish with three shuffles inside the 8-lane group.
@@ -74,9 +75,11 @@ __device__ __forceinline__ float group_sum(float v) {
 
 // NC = ceil(D / 32): float4 output groups per lane.  DC: the head dimension
 // fixed at compile time (so that every shared-memory offset is an immediate
-// and the loops over D unroll), or 0 for any D <= 32 NC.
+// and the loops over D unroll), or 0 for any D <= 32 NC.  Up to D = 64 two
+// CTAs fit an SM's shared memory; the launch bound keeps the registers to
+// match (128 per thread).
 template <int NC, int DC>
-__global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const float* __restrict__ q,
+__global__ void __launch_bounds__(kWarps * 32, NC <= 2 ? 2 : 1) attn_f32_kernel(const float* __restrict__ q,
                                                                const float* __restrict__ k,
                                                                const float* __restrict__ v, float* __restrict__ o,
                                                                float* __restrict__ lse, int Hq, int Hkv, int Nq,
@@ -162,30 +165,40 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const float* __re
     cp_async_wait<1>();  // everything but the group just committed has landed
     group_barrier(bar_id);
 
-    // S = Q K^T: rows rg + 4i, keys g + 8j of the tile
+    // S = Q K^T: rows rg + 4i, keys g + 8j of the tile.  Each score keeps two
+    // partial sums, of its even and of its odd dimensions, as one packed pair:
+    // (x, y) and (z, w) of a float4 are register pairs, so one fma.f32x2 does
+    // two of the products.
     const float* kt = Ks + buf * kBN * KS + g * KS;
-    float s[4][4];
+    uint64_t s2[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
+      for (int j = 0; j < 4; ++j) s2[i][j] = 0;
 #pragma unroll
     for (int d = 0; d < D; d += 4) {
-      float4 a[4], c[4];
+      ulonglong2 a[4], c[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4*>(qw + 4 * i * KS + d);
+      for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const ulonglong2*>(qw + 4 * i * KS + d);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) c[j] = *reinterpret_cast<const float4*>(kt + 8 * j * KS + d);
+      for (int j = 0; j < 4; ++j) c[j] = *reinterpret_cast<const ulonglong2*>(kt + 8 * j * KS + d);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          s[i][j] = fmaf(a[i].x, c[j].x, s[i][j]);
-          s[i][j] = fmaf(a[i].y, c[j].y, s[i][j]);
-          s[i][j] = fmaf(a[i].z, c[j].z, s[i][j]);
-          s[i][j] = fmaf(a[i].w, c[j].w, s[i][j]);
+          s2[i][j] = fma_f32x2(a[i].x, c[j].x, s2[i][j]);
+          s2[i][j] = fma_f32x2(a[i].y, c[j].y, s2[i][j]);
         }
     }
+    float s[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float lo, hi;
+        f2unpack(s2[i][j], lo, hi);
+        s[i][j] = lo + hi;
+      }
     // levels 1-2 per row: running max and sum in base 2, the output rescaled.
     // A tile whose keys every row of the warp sees needs no per-key test.
     const int wq0 = row0 - rg, wq1 = wq0 + kRowsW - 1;  // the warp's first and last query rows
