@@ -21,7 +21,14 @@
  *   fixed scratch array built into the library instead.
  * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *   stream).  Calls are asynchronous: they enqueue kernels on `stream` and
- *   return; results are ready once the stream has been synchronised.
+ *   return; results are ready once the stream has been synchronised, and work
+ *   the caller enqueues after a call in the ordinary way starts after it.
+ *   The attention and split-KV decode kernels allow programmatic dependent
+ *   launch (they signal griddepcontrol.launch_dependents once set up, which
+ *   lets their own merge kernel start early): a kernel the caller launches
+ *   next with programmatic stream serialisation may start before the call's
+ *   outputs are written, and must wait (cudaGridDependencySynchronize) before
+ *   it reads them, as programmatic dependent launch requires in general.
  * - `dtype` names the element type of the 16/32-bit tensors; accumulation is
  *   always fp32.  Softmax scores use natural exponentials; LSE outputs are
  *   natural logarithms of sum_j exp(scale * q.k_j).
