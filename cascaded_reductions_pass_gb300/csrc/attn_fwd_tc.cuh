@@ -73,13 +73,6 @@
 #include <cuda.h>
 #include <math.h>
 
-#ifndef RF_Q_PREFETCH
-#define RF_Q_PREFETCH 1
-#endif
-#ifndef RF_MERGE_PDL
-#define RF_MERGE_PDL 1
-#endif
-
 #include "attn_tc_common.cuh"
 #include "lse_merge.cuh"
 #include "rf_device.cuh"
@@ -857,7 +850,7 @@ cudaError_t launch_cfg(const void* q, const void* k, const void* v, void* o, flo
                                                            Nk, B * Hq, nqt, scale * kLog2e, window, alibi, status,
                                                            static_cast<int>(n_full), split ? plan.n_split : 1,
                                                            o_part, lse_part, rope, rp.pos, batch_major,
-                                                           RF_Q_PREFETCH ? device_sm_count() : 0);
+                                                           device_sm_count());
   err = cudaGetLastError();
   if (err != cudaSuccess || !split) return err;
   const int rows = plan.tail * 2 * kBM;
@@ -871,7 +864,7 @@ cudaError_t launch_cfg(const void* q, const void* k, const void* v, void* o, flo
   lc.stream = s;
   cudaLaunchAttribute la[1];
   la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  la[0].val.programmaticStreamSerializationAllowed = RF_MERGE_PDL;
+  la[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = la;
   lc.numAttrs = 1;
   return cudaLaunchKernelEx(&lc, lse_merge_kernel<DT, AttnTailRows>, static_cast<const float*>(o_part),
