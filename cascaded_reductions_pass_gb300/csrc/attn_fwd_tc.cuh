@@ -233,7 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d_elect(sQ + t * C::kQBytes + bx * (kBM * 128), &tq, &bars->q_full, bx * 64, r0 + t * kBM, bh);
     // With one CTA per SM, CTA id + prefetch_stride is about the one that takes
     // this SM (or another) next: its Q tiles go to L2 now, so that its own
-    // first load, which nothing overlaps, does not wait on HBM.
+    // first load, which nothing overlaps, does not wait on HBM.  Only at
+    // D = 128 (64 KB of Q per unit): there it saves 0.6%; at D = 64 it saved
+    // nothing and part of the prefetched Q was evicted before use (DRAM reads
+    // 88 -> 104 MB at B=4 H=12 N=4096).
     const int nid = id + prefetch_stride;
     if (prefetch_stride > 0 && nid < static_cast<int>(gridDim.x)) {
       const int nunit = MASK == 0 && nid >= n_full ? n_full + (nid - n_full) / n_split : nid;
@@ -850,7 +853,7 @@ cudaError_t launch_cfg(const void* q, const void* k, const void* v, void* o, flo
                                                            Nk, B * Hq, nqt, scale * kLog2e, window, alibi, status,
                                                            static_cast<int>(n_full), split ? plan.n_split : 1,
                                                            o_part, lse_part, rope, rp.pos, batch_major,
-                                                           device_sm_count());
+                                                           D == 128 ? device_sm_count() : 0);
   err = cudaGetLastError();
   if (err != cudaSuccess || !split) return err;
   const int rows = plan.tail * 2 * kBM;
