@@ -59,19 +59,32 @@ __device__ __forceinline__ void fold_block(const uint4& u, Run& r) {
   constexpr int E = Pack<DT>::E;
   float z[E];
   Pack<DT>::unpack(u, z);
-  float bm = z[0];
-#pragma unroll
-  for (int e = 1; e < E; ++e) bm = fmaxf(bm, z[e]);
+  // the block max by 3-input maxima
+  float bm;
+  if constexpr (E == 8) {
+    bm = fmaxf(max3f(z[0], z[1], z[2]), max3f(z[3], z[4], max3f(z[5], z[6], z[7])));
+  } else {
+    static_assert(E == 4, "16-byte blocks of 2- or 4-byte elements");
+    bm = fmaxf(max3f(z[0], z[1], z[2]), z[3]);
+  }
   bm *= kLog2e;
   if (bm > r.m) {  // level 1 moved: correct level 2 by 2^(m_old - m_new)
     r.l *= ex2_ftz(r.m - bm);
     r.m = bm;
   }
   if (r.m == -INFINITY) return;  // nothing finite seen yet (all -inf logits)
-  float s = 0.f;
+  // exponent arguments and the partial sum on packed pairs
+  const uint64_t l2 = f2pack(kLog2e, kLog2e), nm2 = f2pack(-r.m, -r.m);
+  uint64_t s2 = 0;
 #pragma unroll
-  for (int e = 0; e < E; ++e) s += ex2_ftz(fmaf(z[e], kLog2e, -r.m));
-  r.l += s;
+  for (int e = 0; e < E; e += 2) {
+    float x0, x1;
+    f2unpack(fma_f32x2(f2pack(z[e], z[e + 1]), l2, nm2), x0, x1);
+    s2 = add_f32x2(s2, f2pack(ex2_ftz(x0), ex2_ftz(x1)));
+  }
+  float lo, hi;
+  f2unpack(s2, lo, hi);
+  r.l += lo + hi;
 }
 
 // This thread's running (m, l) over the row's 16-byte vectors [c0, c1).
