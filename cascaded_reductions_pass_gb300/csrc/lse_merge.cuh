@@ -62,7 +62,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const float
                                                                      int rows, int S, int D, RowMap out_row,
                                                                      long long out_rows, unsigned* status) {
   __shared__ float s_w[kMergeWarps][kMergeMaxSplits];
-  griddep_wait();  // the kernel that wrote the partials has completed (launched early by the attention split tail)
+  griddep_wait();  // the kernel that wrote the partials has completed (after the attention split tail and the
+                   // split-KV decode this kernel is launched early; otherwise this returns at once)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long row = static_cast<long long>(blockIdx.x) * kMergeWarps + warp;
   if (row >= rows) return;
